@@ -1,0 +1,280 @@
+"""Pins for the CPU oracle: checks against facts fixed by the pages or by mathematics.
+
+Every pin takes the oracle namespace `O` as an argument so the mutation tests can run the
+same pins against copies of the oracle with one planted mistake each.  A pin raises
+AssertionError when it fails.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+def _rand_problem(seed, n_h=3, d_h=5, d_c=7, d_r=4, L=6):
+    r = np.random.default_rng(seed)
+    return dict(
+        q_nope=r.standard_normal((n_h, d_h)), q_rope_raw=r.standard_normal((n_h, d_r)),
+        c_kv=r.standard_normal((L, d_c)), k_rope=r.standard_normal((L, d_r)),
+        w_uk=r.standard_normal((d_c, n_h * d_h)) / math.sqrt(d_c),
+        w_uv=r.standard_normal((d_c, n_h * d_h)) / math.sqrt(d_c),
+        n_h=n_h, d_h=d_h, d_c=d_c, d_r=d_r, L=L)
+
+
+# ------------------------------------------------------------------------------ pages' integers
+
+def pin_cache_sizes_from_pages(O):
+    """The operator-notes page's cache table: 32768 numbers/token for MHA at n_h=d_h=128,
+    512 for MLA at d_c=512, ~32.77 B vs ~0.51 B numbers at 1M context, about 1/64 (~98.4 %)."""
+    g = json.load(open(os.path.join(GOLDEN, "cache_sizes.json")))
+    mha = O.mha_numbers_per_token(g["mha"]["n_h"], g["mha"]["d_h"])
+    mla = O.mla_numbers_per_token(g["mla"]["d_c"])
+    assert mha == g["mha"]["numbers_per_token"]
+    assert mla == g["mla"]["numbers_per_token"]
+    assert round(1_000_000 * mha / 1e9, 2) == g["mha"]["context_1m_billion"]
+    assert round(1_000_000 * mla / 1e9, 2) == g["mla"]["context_1m_billion"]
+    assert mha // mla == g["ratio_denominator"] and mha % mla == 0
+    assert round(100.0 * (1.0 - mla / mha), 1) == g["reduction_percent"]
+    # with the decoupled RoPE key of width 64 the cached row is 576 numbers
+    assert O.mla_numbers_per_token(512, 64) == 576
+
+
+# ------------------------------------------------------------------------------ RoPE
+
+def pin_rope_closed_form(O):
+    """Textbook 2x2 rotation: pair i turns by pos * base^(-2i/d)."""
+    # d=2: theta_0 = 1, so position p is a rotation by p radians.
+    for p in (0, 1, 2.5, 7):
+        got = O.rope_rotate(np.array([1.0, 0.0]), p, 10000.0)
+        assert np.allclose(got, [math.cos(p), math.sin(p)], atol=1e-15)
+        got = O.rope_rotate(np.array([0.0, 1.0]), p, 10000.0)
+        assert np.allclose(got, [-math.sin(p), math.cos(p)], atol=1e-15)
+    # d=4, base 100: theta_1 = 100^(-1/2) = 0.1; only pair 1 is populated.
+    got = O.rope_rotate(np.array([0.0, 0.0, 1.0, 0.0]), 3, 100.0)
+    assert np.allclose(got, [0, 0, math.cos(0.3), math.sin(0.3)], atol=1e-15)
+    # interleaved pairs: the odd element of pair 0 only mixes with element 0
+    got = O.rope_rotate(np.array([0.0, 1.0, 0.0, 0.0]), 1, 100.0)
+    assert np.allclose(got, [-math.sin(1.0), math.cos(1.0), 0, 0], atol=1e-15)
+
+
+def pin_rope_invariants(O):
+    r = np.random.default_rng(11)
+    v = r.standard_normal((5, 64))
+    assert np.array_equal(O.rope_rotate(v, 0, 10000.0), v)           # position 0 = identity
+    pos = r.integers(0, 200000, size=5)
+    w = O.rope_rotate(v, pos, 10000.0)
+    assert np.allclose(np.linalg.norm(w, axis=1), np.linalg.norm(v, axis=1), rtol=1e-12)
+    # composition R(a) R(b) = R(a + b)
+    assert np.allclose(O.rope_rotate(O.rope_rotate(v, 17, 10000.0), 40, 10000.0),
+                       O.rope_rotate(v, 57, 10000.0), atol=1e-11)
+    # relative position: <R_m q, R_n k> depends on m - n only
+    q, k = r.standard_normal(64), r.standard_normal(64)
+    a = O.rope_rotate(q, 1000, 10000.0) @ O.rope_rotate(k, 990, 10000.0)
+    b = O.rope_rotate(q, 10, 10000.0) @ k
+    assert abs(a - b) < 1e-10
+
+
+# ------------------------------------------------------------------------------ projections
+
+def pin_latent_kv_bruteforce(O):
+    """c_kv = x W_DKV (nothing rotated) and k_rope = RoPE(x W_KR) by explicit loops; with
+    d_rope = 2 the rotation angle is the position itself."""
+    r = np.random.default_rng(12)
+    N, dm, dc = 3, 5, 4
+    x, wd, wk = r.standard_normal((N, dm)), r.standard_normal((dm, dc)), r.standard_normal((dm, 2))
+    pos = np.array([0, 3, 11])
+    c, k = O.latent_kv(x, wd, wk, pos, 10000.0)
+    for n in range(N):
+        for j in range(dc):
+            assert abs(c[n, j] - sum(x[n, i] * wd[i, j] for i in range(dm))) < 1e-12
+        a = sum(x[n, i] * wk[i, 0] for i in range(dm))
+        b = sum(x[n, i] * wk[i, 1] for i in range(dm))
+        cs, sn = math.cos(pos[n]), math.sin(pos[n])
+        assert abs(k[n, 0] - (a * cs - b * sn)) < 1e-12
+        assert abs(k[n, 1] - (a * sn + b * cs)) < 1e-12
+
+
+def pin_integer_append_exact(O):
+    """Small-integer x and power-of-two weights at position 0: every product and sum is
+    exact, so the result equals the integer arithmetic exactly."""
+    x = np.array([[1.0, -2.0, 3.0, 0.0]])
+    wd = np.array([[0.5, 1.0], [0.25, -1.0], [2.0, 0.0], [8.0, 4.0]])
+    wk = np.array([[1.0, 0.0], [0.0, 1.0], [0.5, 0.5], [0.0, 0.0]])
+    c, k = O.latent_kv(x, wd, wk, np.array([0]), 10000.0)
+    assert np.array_equal(c, [[0.5 - 0.5 + 6.0, 1.0 + 2.0 + 0.0]])
+    assert np.array_equal(k, [[1.0 + 1.5, -2.0 + 1.5]])
+
+
+def pin_query_projection_bruteforce(O):
+    r = np.random.default_rng(13)
+    n_h, dh, dm = 2, 3, 4
+    x = r.standard_normal((2, dm))
+    wq, wqr = r.standard_normal((dm, n_h * dh)), r.standard_normal((dm, n_h * 2))
+    qn, qr = O.query_projection(x, wq, wqr, np.array([0, 2]), n_h, 10000.0)
+    for n, p in enumerate((0, 2)):
+        for h in range(n_h):
+            for j in range(dh):
+                assert abs(qn[n, h, j] - sum(x[n, i] * wq[i, h * dh + j] for i in range(dm))) < 1e-12
+            a = sum(x[n, i] * wqr[i, h * 2] for i in range(dm))
+            b = sum(x[n, i] * wqr[i, h * 2 + 1] for i in range(dm))
+            assert abs(qr[n, h, 0] - (a * math.cos(p) - b * math.sin(p))) < 1e-12
+            assert abs(qr[n, h, 1] - (a * math.sin(p) + b * math.cos(p))) < 1e-12
+
+
+# ------------------------------------------------------------------------------ attention
+
+def pin_attention_bruteforce(O):
+    """Un-absorbed attention with explicit loops over heads, tokens and dims (math.exp)."""
+    P = _rand_problem(14, n_h=2, d_h=2, d_c=3, d_r=2, L=3)
+    n_h, d_h, d_c, d_r, L = P["n_h"], P["d_h"], P["d_c"], P["d_r"], P["L"]
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    qn, qr, c, kr, wuk, wuv = (P["q_nope"], P["q_rope_raw"], P["c_kv"], P["k_rope"],
+                               P["w_uk"], P["w_uv"])
+    o, o_lat, lse, _ = O.attention_unabsorbed(qn, qr, c, kr, wuk, wuv, scale)
+    for h in range(n_h):
+        s = []
+        for t in range(L):
+            dot = 0.0
+            for j in range(d_h):
+                k = sum(c[t, cc] * wuk[cc, h * d_h + j] for cc in range(d_c))
+                dot += qn[h, j] * k
+            dot += sum(qr[h, i] * kr[t, i] for i in range(d_r))
+            s.append(dot * scale)
+        z = sum(math.exp(v) for v in s)
+        assert abs(lse[h] - math.log(z)) < 1e-12
+        p = [math.exp(v) / z for v in s]
+        for j in range(d_h):
+            ref = sum(p[t] * sum(c[t, cc] * wuv[cc, h * d_h + j] for cc in range(d_c))
+                      for t in range(L))
+            assert abs(o[h, j] - ref) < 1e-12
+        for cc in range(d_c):
+            assert abs(o_lat[h, cc] - sum(p[t] * c[t, cc] for t in range(L))) < 1e-12
+
+
+def pin_attention_closed_forms(O):
+    P = _rand_problem(15)
+    n_h, d_h, d_c, d_r, L = P["n_h"], P["d_h"], P["d_c"], P["d_r"], P["L"]
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    wuk, wuv = P["w_uk"], P["w_uv"]
+    # one token: p = 1, o = V[0], o_lat = c_kv[0]
+    o, o_lat, lse, _ = O.attention_unabsorbed(P["q_nope"], P["q_rope_raw"], P["c_kv"][:1],
+                                              P["k_rope"][:1], wuk, wuv, scale)
+    V0 = (P["c_kv"][:1] @ wuv).reshape(n_h, d_h)
+    assert _rel(o, V0) < 1e-13 and _rel(o_lat, np.repeat(P["c_kv"][:1], n_h, 0)) < 1e-13
+    # zero query: uniform weights, lse = ln L, o_lat = mean of the latents
+    o, o_lat, lse, _ = O.attention_unabsorbed(np.zeros((n_h, d_h)), np.zeros((n_h, d_r)),
+                                              P["c_kv"], P["k_rope"], wuk, wuv, scale)
+    assert np.allclose(lse, math.log(L), atol=1e-14)
+    assert _rel(o_lat, np.repeat(P["c_kv"].mean(0, keepdims=True), n_h, 0)) < 1e-13
+    # all rows equal with a known score: c_kv = e0, k_rope = e0, W_UK[0, h*d_h] = a,
+    # q_nope[h] = b e0, q_rope[h] = g e0  ->  s = (a b + g) * scale, lse = s + ln L
+    a, b, g = 1.5, -0.75, 2.0
+    c = np.zeros((L, d_c)); c[:, 0] = 1.0
+    kr = np.zeros((L, d_r)); kr[:, 0] = 1.0
+    wk = np.zeros((d_c, n_h * d_h)); wk[0, ::d_h] = a
+    qn = np.zeros((n_h, d_h)); qn[:, 0] = b
+    qr = np.zeros((n_h, d_r)); qr[:, 0] = g
+    _, o_lat, lse, _ = O.attention_unabsorbed(qn, qr, c, kr, wk, wuv, scale)
+    assert np.allclose(lse, (a * b + g) * scale + math.log(L), atol=1e-14)
+    assert np.allclose(o_lat, np.repeat(c[:1], n_h, 0), atol=1e-15)
+    # two tokens with scores differing by d: p0 = 1 / (1 + e^{-d})
+    c2 = np.zeros((2, d_c)); c2[0, 0] = 1.0; c2[1, 1] = 1.0
+    kr2 = np.zeros((2, d_r))
+    wk2 = np.zeros((d_c, n_h * d_h)); wk2[0, ::d_h] = 1.0
+    qn2 = np.zeros((n_h, d_h)); qn2[:, 0] = 3.0 / scale
+    _, o_lat, lse, _ = O.attention_unabsorbed(qn2, np.zeros((n_h, d_r)), c2, kr2, wk2, wuv, scale)
+    p0 = 1.0 / (1.0 + math.exp(-3.0))
+    assert np.allclose(o_lat[:, 0], p0, atol=1e-14) and np.allclose(o_lat[:, 1], 1 - p0, atol=1e-14)
+    assert np.allclose(lse, math.log(math.exp(3.0) + 1.0), atol=1e-14)
+
+
+def pin_softmax_properties(O):
+    r = np.random.default_rng(16)
+    s = r.standard_normal((4, 9)) * 5
+    p, lse = O.softmax_lse(s)
+    assert np.allclose(p.sum(-1), 1.0, atol=1e-14)
+    p2, lse2 = O.softmax_lse(s + 123.0)
+    assert np.allclose(p2, p, atol=1e-14) and np.allclose(lse2, lse + 123.0, atol=1e-12)
+    s[:, 3] = -np.inf
+    p3, _ = O.softmax_lse(s)
+    assert np.all(p3[:, 3] == 0.0)
+    assert np.allclose(np.log(np.exp(s[0, np.isfinite(s[0])]).sum()), O.softmax_lse(s)[1][0])
+
+
+def pin_absorbed_equals_unabsorbed(O):
+    """Associativity (rmj dispatch; glossary absorption paragraph): folding W_UK into the
+    query and W_UV into the output gives the same attention as restoring K and V."""
+    for seed, kw in ((21, {}), (22, dict(n_h=4, d_h=8, d_c=16, d_r=4, L=37)),
+                     (23, dict(n_h=1, d_h=3, d_c=2, d_r=2, L=1))):
+        P = _rand_problem(seed, **kw)
+        d_h, d_c, d_r = P["d_h"], P["d_c"], P["d_r"]
+        scale = 1.0 / math.sqrt(d_h + d_r)
+        pos = 5
+        qr_rot = O.rope_rotate(P["q_rope_raw"], pos, 10000.0)
+        o, o_lat, lse, _ = O.attention_unabsorbed(P["q_nope"], qr_rot, P["c_kv"], P["k_rope"],
+                                                  P["w_uk"], P["w_uv"], scale)
+        q_cat = O.absorb_query(P["q_nope"][None], P["q_rope_raw"][None], np.array([pos]),
+                               P["w_uk"], 10000.0)[0]
+        rows = np.concatenate([P["c_kv"], P["k_rope"]], axis=1)
+        o_lat2, lse2 = O.attention_latent(q_cat, rows, d_c, scale)
+        o2 = O.up_project_output(o_lat2[None], P["w_uv"])[0]
+        assert _rel(o_lat2, o_lat) < 1e-10
+        assert np.max(np.abs(lse2 - lse)) < 1e-10
+        assert _rel(o2, o.reshape(-1)) < 1e-10
+
+
+def pin_causal_prefill(O):
+    """Row i of the masked [T, T] prefill equals single-query attention over tokens 0..i."""
+    r = np.random.default_rng(24)
+    T, n_h, d_h, d_c, d_r = 7, 2, 3, 5, 4
+    qn, qr = r.standard_normal((T, n_h, d_h)), r.standard_normal((T, n_h, d_r))
+    c, kr = r.standard_normal((T, d_c)), r.standard_normal((T, d_r))
+    wuk, wuv = r.standard_normal((d_c, n_h * d_h)), r.standard_normal((d_c, n_h * d_h))
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    o, o_lat, lse = O.causal_prefill_unabsorbed(qn, qr, c, kr, wuk, wuv, scale)
+    for i in range(T):
+        oi, oli, lsei, _ = O.attention_unabsorbed(qn[i], qr[i], c[:i + 1], kr[:i + 1], wuk, wuv,
+                                                  scale)
+        assert _rel(o[i], oi) < 1e-12 and _rel(o_lat[i], oli) < 1e-12
+        assert np.max(np.abs(lse[i] - lsei)) < 1e-12
+    # query 0 sees only token 0: o_lat = c_kv[0]
+    assert _rel(o_lat[0], np.repeat(c[:1], n_h, 0)) < 1e-13
+
+
+def pin_output_projection_bruteforce(O):
+    r = np.random.default_rng(25)
+    o = r.standard_normal((2, 3, 2))          # [N, n_h, d_h]
+    wo = r.standard_normal((6, 4))
+    out = O.output_projection(o, wo)
+    for n in range(2):
+        for j in range(4):
+            ref = sum(o[n, h, d] * wo[h * 2 + d, j] for h in range(3) for d in range(2))
+            assert abs(out[n, j] - ref) < 1e-12
+    # head slice: o_lat @ W_UV_h by loops
+    ol = r.standard_normal((1, 2, 3))
+    wuv = r.standard_normal((3, 2 * 4))
+    up = O.up_project_output(ol, wuv)
+    for h in range(2):
+        for j in range(4):
+            assert abs(up[0, h * 4 + j] - sum(ol[0, h, c] * wuv[c, h * 4 + j] for c in range(3))) < 1e-12
+
+
+def pin_paged_gather(O):
+    """Token t of a sequence lives in page table[t // page_size], slot t % page_size."""
+    pool = np.arange(5 * 4 * 2, dtype=np.float64).reshape(5, 4, 2)
+    rows = O.sequence_rows(pool, np.array([3, 0, 4]), 10)
+    for t in range(10):
+        assert np.array_equal(rows[t], pool[[3, 0, 4][t // 4], t % 4])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
