@@ -1,0 +1,372 @@
+"""Benchmark of the MLA latent-KV decode hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the hot path over one batch: mla_absorb_q -> mla_decode (split-K
+attention + log-sum-exp combine) -> mla_out, on the DeepSeek-V2-shaped decode batch
+(B=16, 4096 cached tokens each, 128 heads, d_c=512, d_rope=64, page size 64, shuffled pages).
+Inputs are synthetic and resident in HBM; L2 is flushed (a 256 MB write) between steps.
+With --gpus N > 1 (launched by torchrun) every rank runs an independent replica (the path
+shards by sequence with no exchange), and value is the job total.
+
+--impl reference times the CPU float64 oracle on bounded samples of the same workload.
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_workloads as W  # noqa: E402
+
+METRIC = "MLA decode tokens/s, HBM GB/s and % of roofline (B=16, T=4096, 128 heads)"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def workload_numbers(case):
+    """Algorithmic bytes and FLOPs of one decode launch (the split-attention kernel):
+    cache rows read once (L*W*2), queries (n_h*W*2), outputs (n_h*(d_c*2+4)) per sequence;
+    FLOPs 2*L*n_h*(W + d_c) per sequence (scores plus weighted sum)."""
+    s = case["shape"]
+    L = case["seq_lens"].astype(np.int64)
+    Wd = s.width
+    bytes_ = int(np.sum(L * Wd * 2 + s.n_heads * Wd * 2 + s.n_heads * (s.d_latent * 2 + 4)))
+    flops = int(np.sum(2 * L * s.n_heads * (Wd + s.d_latent)))
+    return bytes_, flops
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_79_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, workload: str):
+    """DRAM traffic per launch from a committed ncu summary, or None when the kernel sources
+    changed since that capture."""
+    p = os.path.join(PROFILE_DIR, f"{kernel_key}_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_digest") != source_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2])); power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------------------ reference arm
+
+def cpu_oracle_sample(case, n_seq: int):
+    """Time the float64 oracle (un-absorbed: restore K and V, softmax attention, W_UV folded
+    in by V) on the first n_seq sequences with all heads.  Returns seconds."""
+    import oracle.mla_oracle as O
+    s = case["shape"]
+    sc = O.default_scale(s.d_nope, s.d_rope)
+    pool = case["pool"]
+    f = lambda a: W.to_f64(a, case["dtype"])  # noqa: E731
+    w_uk, w_uv = f(case["w_uk"]), f(case["w_uv"])
+    t0 = time.perf_counter()
+    for b in range(n_seq):
+        L = int(case["seq_lens"][b])
+        rows = W.to_f64(W.gather_rows(pool, case["page_table"][b], L), case["dtype"])
+        q_r = O.rope_rotate(f(case["q_rope"][b]), case["pos"][b], s.rope_base)
+        O.attention_unabsorbed(f(case["q_nope"][b]), q_r, rows[:, :s.d_latent], rows[:, s.d_latent:],
+                               w_uk, w_uv, sc)
+    return time.perf_counter() - t0
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    case = W.make_workload(args.workload)
+    for _ in range(max(0, args.warmup)):
+        cpu_oracle_sample(case, 1)
+    ts = [cpu_oracle_sample(case, 1) for _ in range(args.steps)]
+    t = sum(ts)
+    value = args.steps / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(args.workload, case),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                         "sample": "one sequence (4096 cached tokens, all 128 heads) per step, "
+                                   "un-absorbed float64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(name, case):
+    s = case["shape"]
+    return {"workload": name, "batch": int(case["seq_lens"].shape[0]),
+            "seq_len": int(case["seq_lens"].max()), "n_heads": s.n_heads, "d_nope": s.d_nope,
+            "d_rope": s.d_rope, "d_latent": s.d_latent, "page_size": s.page_size,
+            "page_table": "shuffled", "l2": "flushed between steps (256 MB write)"}
+
+
+# ------------------------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from mla_latent_kv_79_b300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    import mla_latent_kv_79_b300 as M
+
+    case = W.make_workload(args.workload)
+    s = case["shape"]
+    cfg = M.MLAConfig.from_shape(s, case["dtype"])
+    dt = case["dtype"]
+    dev = lambda a: W.to_device(a, dt)  # noqa: E731
+    cache = M.PagedCache(dev(case["pool"]), torch.from_numpy(case["page_table"]).cuda(),
+                         torch.from_numpy(case["seq_lens"]).cuda())
+    q_nope, q_rope = dev(case["q_nope"]), dev(case["q_rope"])
+    pos = torch.from_numpy(case["pos"]).cuda()
+    w_uk, w_uv = dev(case["w_uk"]), dev(case["w_uv"])
+    B = int(case["seq_lens"].shape[0])
+    q_cat = torch.empty((B, s.n_heads, s.width), dtype=cfg.torch_dtype, device="cuda")
+    o_lat = torch.empty((B, s.n_heads, s.d_latent), dtype=cfg.torch_dtype, device="cuda")
+    lse = torch.empty((B, s.n_heads), dtype=torch.float32, device="cuda")
+    o = torch.empty((B, s.n_heads * s.d_nope), dtype=cfg.torch_dtype, device="cuda")
+    ws = M.alloc_workspace(cfg)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        M.mla_absorb_q(cfg, q_nope, q_rope, pos, w_uk, q_cat=q_cat, stream=stream)
+        M.mla_decode(cfg, cache, q_cat, o_lat=o_lat, lse=lse, workspace=ws, stream=stream)
+        M.mla_out(cfg, o_lat, w_uv, o=o, stream=stream)
+
+    warm = max(3, args.warmup)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(warm):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert M.mla_get_device_error() == 0
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in kev:  # create the events so their handles exist
+        a.record(); b.record()
+    torch.cuda.synchronize()
+    lib = M.lib()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = lib.mla_kernel_launches()
+    for i in range(K):
+        flush.zero_()
+        lib.mla_set_attention_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    lib.mla_set_attention_events(None, None)
+    torch.cuda.synchronize()
+    launches = lib.mla_kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    path = M.mla_last_attention_path()
+    assert M.mla_get_device_error() == 0
+
+    # end to end through host buffers: per step, copy the step's queries in from pinned
+    # host memory and read the output back
+    h_qn = q_nope.cpu().pin_memory()
+    h_qr = q_rope.cpu().pin_memory()
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        eev[i][0].record(stream)
+        q_nope.copy_(h_qn, non_blocking=True)
+        q_rope.copy_(h_qr, non_blocking=True)
+        step()
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clock = clocks.stop()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        dist.barrier()
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    alg_bytes, alg_flops = workload_numbers(case)
+    hbm, tflops, src = peaks()
+    k_mean_s = (sum(kern_ms) / K) * 1e-3
+    achieved = alg_bytes / k_mean_s / 1e9
+    kernel_key = "tc_attention" if path == 2 else "simt_attention"
+    tokens_total = B * K * world
+    line = {
+        "metric": METRIC,
+        "value": tokens_total / (total_ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": warm,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config_of(args.workload, case),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": ncu_traffic(kernel_key, args.workload),
+                     "kernel": kernel_key, "kernel_us": k_mean_s * 1e6,
+                     "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
+                     "tflops": alg_flops / k_mean_s / 1e12, "peak_source": src,
+                     "tensor_frac": alg_flops / k_mean_s / 1e12 / tflops,
+                     "roofline_us": 1e6 * max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12))},
+        "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size()),
+                "d2h_bytes_per_step": int(h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size())},
+        "gpu_launches": int(launches),
+        "clocks": clock,
+        "step_us_median": 1e3 * statistics.median(step_ms),
+    }
+    if not args.no_cpu_baseline:
+        n_seq = 0
+        t_cpu = 0.0
+        while n_seq < B and t_cpu < 10.0:
+            t_cpu += cpu_oracle_sample(dict(case, seq_lens=case["seq_lens"][n_seq:],
+                                             page_table=case["page_table"][n_seq:],
+                                             q_nope=case["q_nope"][n_seq:], q_rope=case["q_rope"][n_seq:],
+                                             pos=case["pos"][n_seq:]), 1)
+            n_seq += 1
+        line["cpu_baseline"] = {"value": n_seq / t_cpu, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                                "sample": f"{n_seq} of {B} sequences (all 128 heads, 4096 cached tokens), "
+                                          "un-absorbed float64 oracle"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_b16_l4096", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

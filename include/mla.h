@@ -1,0 +1,189 @@
+/*
+ * mla.h - C ABI of libmla: the data-parallel hot path of Multi-head Latent Attention (MLA)
+ * over a paged latent KV cache, for NVIDIA B300 (sm_103a).
+ *
+ * Sources (page title, section):
+ *   [OPN] "Operator Notes (1): MLA - Multi-head Latent Attention at the Operator Level",
+ *         section 2 (weight shapes W_DKV [d_model,d_c], W_UK/W_UV [d_c,n_h*d_h],
+ *         the chain c_kv = x W_DKV, K = c_kv W_UK, V = c_kv W_UV, softmax(Q K^T/sqrt d) V),
+ *         section 3 (only c_kv enters the cache).
+ *   [GLO] "multi-head latent attention" glossary: a small decoupled RoPE key is cached beside
+ *         the latent; the up-projections are absorbed into the query and output projections;
+ *         MLA pairs with PagedAttention.
+ *   [RMJ] "Multi-Head Latent Attention and the Compression of the KV Cache": by associativity
+ *         the up-projection is absorbed into the query, so attention runs on the latent.
+ *
+ * Notation: n_h heads, d_h (= d_nope) per-head width, d_r (= d_rope) RoPE width, d_c latent
+ * width, W = d_c + d_r numbers cached per token, P = page_size tokens per page.
+ *
+ * Conventions that hold for every entry point:
+ *   - Every pointer named "device" is CUDA device memory owned by the caller; the library
+ *     never allocates, frees or retains it.  Host pointers are read before the call returns.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  The returned status
+ *     covers host-side argument checks and launch errors only.  Faults found on the device
+ *     (a page id outside the pool, a position beyond the page table, a bounded wait that ran
+ *     out) are recorded in a per-device error word and read with mla_get_device_error().
+ *   - Element type of every floating-point tensor is cfg->dtype (MLA_F32 or MLA_BF16), except
+ *     lse, which is always float32.  bf16 is stored as IEEE bfloat16 bits.
+ *   - Every tensor pointer must be 16-byte aligned; tensors are dense row-major with the
+ *     shapes given below (no strides).
+ *   - RoPE rotates interleaved pairs (2i, 2i+1) by pos * rope_base^(-2i/d_r); positions are
+ *     0-based.  The score scale is cfg->softmax_scale, or 1/sqrt(d_h + d_r) when it is 0.
+ *   - Slots of the pool that no token owns must hold finite values (masked tokens still
+ *     meet a zero weight: 0 * finite = 0).
+ *   - lse is the natural-log log-sum-exp of the scaled scores of one (query, head).
+ *
+ * Error behaviour: a non-OK status means nothing was launched, except MLA_ERR_CUDA, which
+ * reports the CUDA error of a launch (cudaGetLastError is cleared).
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size or dimension          */
+    MLA_ERR_UNSUPPORTED = 2,    /* dimensions this build does not handle                    */
+    MLA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed                     */
+    MLA_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query returned */
+    MLA_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait ran out (device error word)   */
+    MLA_ERR_DEVICE_BOUNDS = 6   /* a page id / position outside the cache (device error word) */
+} mla_status;
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Model dimensions ([OPN] section 2 conventions, plus the decoupled RoPE width of [GLO]). */
+typedef struct {
+    int32_t n_heads;       /* n_h                                   */
+    int32_t d_nope;        /* d_h: per-head query/key width without RoPE */
+    int32_t d_rope;        /* d_r: width of the decoupled RoPE key (even) */
+    int32_t d_latent;      /* d_c: latent width, the cached c_kv      */
+    int32_t d_model;       /* hidden width of x                       */
+    int32_t page_size;     /* P: tokens per cache page                */
+    float rope_base;       /* RoPE base, e.g. 10000                   */
+    float softmax_scale;   /* 0 => 1/sqrt(d_nope + d_rope)            */
+    int32_t dtype;         /* mla_dtype                               */
+} mla_config;
+
+/* Paged latent cache ([GLO]: MLA pairs with PagedAttention; [OPN] s.3: only c_kv is cached,
+ * here with the RoPE key beside it).  Token t of sequence b lives in row
+ * pool[page_table[b*max_pages + t/P]][t%P][0:W]: columns [0,d_c) hold c_kv, [d_c,W) the
+ * rotated RoPE key. */
+typedef struct {
+    void* pool;                 /* device [num_pages, P, W], cfg->dtype                 */
+    int64_t num_pages;
+    const int32_t* page_table;  /* device [batch, max_pages] physical page ids         */
+    int32_t max_pages;
+    int32_t batch;
+    const int32_t* seq_lens;    /* device [batch]: cached tokens of each sequence       */
+} mla_cache;
+
+/* Build identification: returns MLA_ABI_VERSION. */
+#define MLA_ABI_VERSION 1
+MLA_API int32_t mla_abi_version(void);
+
+/* Short English text for a status code (static storage). */
+MLA_API const char* mla_status_string(mla_status status);
+
+/* mla_cache_append - write new tokens into the latent cache.
+ * [OPN] s.2 "c_kv = x @ W_DKV" (the only KV state cached) and [GLO] decoupled RoPE key:
+ *   row = [ x[n] @ W_DKV | RoPE(x[n] @ W_KR, pos[n]) ]   (fp32 accumulation, rounded to dtype)
+ *   stored to pool[page_table[seq_idx[n]][pos[n]/P]][pos[n]%P].
+ * x       device [n_tokens, d_model]
+ * w_dkv   device [d_model, d_c]       w_kr device [d_model, d_r]
+ * seq_idx device int32 [n_tokens]     pos  device int32 [n_tokens]
+ * Tokens must target distinct rows.  seq_lens is not modified (the caller owns lengths).
+ * A seq_idx outside [0,batch), a position outside the page table or a page id outside the
+ * pool sets MLA_ERR_DEVICE_BOUNDS and that token is skipped.  n_tokens == 0 is a no-op. */
+MLA_API mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const void* x,
+                            const void* w_dkv, const void* w_kr, const int32_t* seq_idx,
+                            const int32_t* pos, int32_t n_tokens, mla_stream_t stream);
+
+/* mla_absorb_q - absorbed query ([GLO] absorption paragraph, [RMJ] associativity):
+ *   q_cat[n,h,0:d_c]  = q_nope[n,h,:] @ W_UK[:, h*d_h:(h+1)*d_h]^T
+ *   q_cat[n,h,d_c:W]  = RoPE(q_rope[n,h,:], pos[n])
+ * q_nope device [n_tokens, n_h, d_h]   q_rope device [n_tokens, n_h, d_r] (not rotated)
+ * pos    device int32 [n_tokens]       w_uk   device [d_c, n_h*d_h]
+ * q_cat  device [n_tokens, n_h, W] (output).  n_tokens == 0 is a no-op. */
+MLA_API mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q_rope,
+                        const int32_t* pos, const void* w_uk, void* q_cat, int32_t n_tokens,
+                        mla_stream_t stream);
+
+/* Bytes of device workspace that mla_decode / mla_prefill need on the current device for
+ * this configuration (split partials).  The same buffer serves both and may be reused by
+ * calls that do not overlap in time. */
+MLA_API mla_status mla_workspace_size(const mla_config* cfg, size_t* bytes);
+
+/* mla_decode - one query token per sequence over its whole cached prefix ([OPN] s.2 scores,
+ * softmax, weighted sum, in the absorbed form of [GLO]/[RMJ]):
+ *   s[b,h,t]  = (q_cat[b,h,:] . pool_row(b,t)) * scale         for t < seq_lens[b]
+ *   lse[b,h]  = log sum_t exp(s[b,h,t])
+ *   o_lat[b,h,:] = sum_t exp(s[b,h,t] - lse[b,h]) * pool_row(b,t)[0:d_c]
+ * q_cat device [batch, n_h, W]; o_lat device [batch, n_h, d_c]; lse device float [batch, n_h].
+ * The work is split over the sequence length and merged by a log-sum-exp combine.
+ * A sequence with seq_lens[b] == 0 yields o_lat = 0 and lse = -inf.
+ * workspace: device, at least mla_workspace_size() bytes (else MLA_ERR_WORKSPACE). */
+MLA_API mla_status mla_decode(const mla_config* cfg, const mla_cache* cache, const void* q_cat,
+                      void* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+                      mla_stream_t stream);
+
+/* mla_prefill - causal attention of n_queries consecutive tokens of sequence `seq` against
+ * that sequence's cache ([OPN] s.2 prefill chain with the causal mask of autoregressive
+ * attention): query i sits at position q_start + i and sees tokens t <= q_start + i, which
+ * must already be in the cache (append first).  Same formulas and outputs as mla_decode:
+ * q_cat device [n_queries, n_h, W]; o_lat device [n_queries, n_h, d_c];
+ * lse device float [n_queries, n_h]; workspace as for mla_decode. */
+MLA_API mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, int32_t seq,
+                       int32_t q_start, int32_t n_queries, const void* q_cat, void* o_lat,
+                       float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* mla_out - absorbed output up-projection ([OPN] s.2 "V = c_kv @ W_UV", folded into the
+ * output side as [GLO] describes):  o[n, h*d_h:(h+1)*d_h] = o_lat[n,h,:] @ W_UV[:, h*d_h:(h+1)*d_h]
+ * o_lat device [n_tokens, n_h, d_c]; w_uv device [d_c, n_h*d_h]; o device [n_tokens, n_h*d_h].
+ * n_tokens == 0 is a no-op. */
+MLA_API mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, void* o,
+                   int32_t n_tokens, mla_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Returns MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_CUDA. */
+MLA_API mla_status mla_get_device_error(mla_stream_t stream);
+
+/* Process-wide tuning / test knobs (not needed for normal use).  Returns the previous value. */
+typedef enum {
+    MLA_TUNE_ATTN_UNITS = 0,   /* >0: number of split units for decode/prefill (test use)    */
+    MLA_TUNE_FORCE_SIMT = 1,   /* 1: run the portable SIMT kernels even where tcgen05 applies */
+    MLA_TUNE_WAIT_LIMIT_US = 2 /* device bounded-wait limit in microseconds (default 2e6)   */
+} mla_tuning_key;
+MLA_API int32_t mla_set_tuning(int32_t key, int32_t value);
+
+/* Timing hook for benchmarks: when both are non-NULL, the next mla_decode / mla_prefill
+ * calls on this thread record `before` (a cudaEvent_t) on their stream immediately before
+ * the split-attention kernel and `after` immediately after it, so the caller can time that
+ * kernel alone.  Pass NULLs to stop.  The events stay owned by the caller. */
+MLA_API void mla_set_attention_events(void* before, void* after);
+
+/* Number of CUDA kernels this process has launched through libmla so far. */
+MLA_API uint64_t mla_kernel_launches(void);
+
+/* Which kernel family the last mla_decode/mla_prefill call on this thread used:
+ * 0 none yet, 1 SIMT, 2 tcgen05. */
+MLA_API int32_t mla_last_attention_path(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H */

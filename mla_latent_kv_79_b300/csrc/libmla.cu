@@ -1,0 +1,353 @@
+// libmla: C ABI of the MLA latent-KV hot path (declarations and contracts in include/mla.h).
+//
+// One translation unit holds every kernel so the per-device error word is a single symbol.
+#include <cuda_runtime.h>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "mla.h"
+#include "mla_common.cuh"
+#include "sched.cuh"
+#include "simt_gemm.cuh"
+#include "simt_attention.cuh"
+#include "tc_attention.cuh"
+
+namespace mla {
+
+// ----------------------------------------------------------------------------- device info
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0, smem_optin = 0, cc_major = 0, cc_minor = 0;
+};
+static DeviceInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+static mla_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!d.ready) {
+            if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+                return MLA_ERR_CUDA;
+            d.ready = true;
+        }
+    }
+    *out = &d;
+    return MLA_OK;
+}
+
+// ----------------------------------------------------------------------------- knobs
+static std::atomic<int> g_tune[3] = {{0}, {0}, {2000000}};
+static thread_local int g_last_path = 0;
+static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+static std::atomic<unsigned long long> g_launches{0};
+
+static void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static size_t elem_size(const mla_config* c) { return c->dtype == MLA_BF16 ? 2 : 4; }
+
+static mla_status check_config(const mla_config* c) {
+    if (!c) return MLA_ERR_INVALID_ARG;
+    if (c->dtype != MLA_F32 && c->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+    if (c->n_heads <= 0 || c->d_nope <= 0 || c->d_rope <= 0 || c->d_latent <= 0 ||
+        c->d_model <= 0 || c->page_size <= 0)
+        return MLA_ERR_INVALID_ARG;
+    if ((c->d_rope & 1) || (c->d_latent & 1)) return MLA_ERR_INVALID_ARG;
+    if (!(c->rope_base > 0.f) || !std::isfinite(c->rope_base)) return MLA_ERR_INVALID_ARG;
+    if (c->softmax_scale < 0.f || !std::isfinite(c->softmax_scale)) return MLA_ERR_INVALID_ARG;
+    // row widths in bytes must keep 16-byte alignment of every row
+    const size_t es = elem_size(c);
+    if (((size_t)(c->d_latent + c->d_rope) * es) % 16 || ((size_t)c->d_latent * es) % 16)
+        return MLA_ERR_UNSUPPORTED;
+    if (c->d_latent + c->d_rope > 1024 || c->d_latent > 1024) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+static mla_status check_cache(const mla_config* c, const mla_cache* k) {
+    if (!k || !k->pool || !k->page_table || k->num_pages <= 0 || k->max_pages <= 0 || k->batch <= 0)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(k->pool)) return MLA_ERR_INVALID_ARG;
+    if ((long long)k->max_pages * c->page_size > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+static float scale_of(const mla_config* c) {
+    return c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / std::sqrt((double)(c->d_nope + c->d_rope)));
+}
+
+static mla_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+static int max_units(const DeviceInfo* d) { return d->sms > 0 ? d->sms : 148; }
+
+// ----------------------------------------------------------------------------- attention
+static mla_status attention(const mla_config* cfg, const mla_cache* cache, QuerySet qs,
+                            const void* q_cat, void* o_lat, float* lse, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+    DeviceInfo* dev;
+    mla_status st = device_info(&dev);
+    if (st != MLA_OK) return st;
+    if (qs.n_queries == 0) return MLA_OK;
+    if (!q_cat || !o_lat || !lse || !aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    size_t need = 0;
+    mla_workspace_size(cfg, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return MLA_ERR_WORKSPACE;
+
+    const int n_h = cfg->n_heads, d_c = cfg->d_latent, W = cfg->d_latent + cfg->d_rope;
+    const int U_max = max_units(dev);
+    AttnArgs a;
+    a.qs = qs;
+    a.q_cat = q_cat;
+    a.pool = cache->pool;
+    a.page_table = cache->page_table;
+    a.max_pages = cache->max_pages;
+    a.num_pages = cache->num_pages;
+    a.o_lat = o_lat;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = a.part_o + (size_t)2 * U_max * n_h * d_c;
+    a.n_h = n_h;
+    a.d_c = d_c;
+    a.width = W;
+    a.scale = scale_of(cfg);
+
+    const int forced = g_tune[MLA_TUNE_ATTN_UNITS].load();
+    const bool use_tc = !g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_attention_supported(cfg, cache, dev->cc_major, dev->cc_minor);
+    const bool timed = g_ev_before && g_ev_after;
+    if (use_tc) {
+        int U = forced > 0 ? (forced < U_max / 2 ? forced : U_max / 2) : U_max / 2;
+        a.n_units = U;
+        if (timed) cudaEventRecord(g_ev_before, stream);
+        st = tc_attention_launch(a, cache, (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull, stream);
+        if (timed) cudaEventRecord(g_ev_after, stream);
+        if (st != MLA_OK) return st;
+        count_launches(1);
+        g_last_path = 2;
+    } else {
+        int hg = n_h < 16 ? n_h : 16;
+        size_t smem = simt_attn_smem_bytes(hg, W, d_c);
+        while (smem > (size_t)dev->smem_optin && hg > 1) { hg /= 2; smem = simt_attn_smem_bytes(hg, W, d_c); }
+        if (smem > (size_t)dev->smem_optin) return MLA_ERR_UNSUPPORTED;
+        int U = forced > 0 ? (forced < U_max ? forced : U_max) : U_max;
+        a.n_units = U;
+        dim3 grid(U, (n_h + hg - 1) / hg);
+        if (timed) cudaEventRecord(g_ev_before, stream);
+        if (cfg->dtype == MLA_BF16) {
+            cudaFuncSetAttribute(simt_attention_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            simt_attention_kernel<bf16><<<grid, 256, smem, stream>>>(a, hg);
+        } else {
+            cudaFuncSetAttribute(simt_attention_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            simt_attention_kernel<float><<<grid, 256, smem, stream>>>(a, hg);
+        }
+        if (timed) cudaEventRecord(g_ev_after, stream);
+        if ((st = launch_status()) != MLA_OK) return st;
+        count_launches(1);
+        g_last_path = 1;
+    }
+    dim3 cgrid(qs.n_queries, (n_h + 7) / 8);
+    if (cfg->dtype == MLA_BF16) combine_kernel<bf16><<<cgrid, 256, 0, stream>>>(a);
+    else combine_kernel<float><<<cgrid, 256, 0, stream>>>(a);
+    count_launches(1);
+    return launch_status();
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char* mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported dimensions";
+        case MLA_ERR_CUDA: return "CUDA error";
+        case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MLA_ERR_DEVICE_TIMEOUT: return "device bounded wait timed out";
+        case MLA_ERR_DEVICE_BOUNDS: return "page id or position outside the cache";
+    }
+    return "unknown status";
+}
+
+int32_t mla_set_tuning(int32_t key, int32_t value) {
+    if (key < 0 || key > 2) return -1;
+    if (key == MLA_TUNE_WAIT_LIMIT_US && value <= 0) value = 2000000;
+    return g_tune[key].exchange(value);
+}
+
+int32_t mla_last_attention_path(void) { return g_last_path; }
+
+void mla_set_attention_events(void* before, void* after) {
+    g_ev_before = reinterpret_cast<cudaEvent_t>(before);
+    g_ev_after = reinterpret_cast<cudaEvent_t>(after);
+}
+
+uint64_t mla_kernel_launches(void) { return g_launches.load(); }
+
+mla_status mla_workspace_size(const mla_config* cfg, size_t* bytes) {
+    if (!bytes) return MLA_ERR_INVALID_ARG;
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    const size_t slots = 2 * (size_t)max_units(dev);
+    size_t b = slots * (size_t)cfg->n_heads * ((size_t)cfg->d_latent + 1) * sizeof(float);
+    *bytes = (b + 255) & ~(size_t)255;
+    return MLA_OK;
+}
+
+mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const void* x,
+                            const void* w_dkv, const void* w_kr, const int32_t* seq_idx,
+                            const int32_t* pos, int32_t n_tokens, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if ((st = check_cache(cfg, cache)) != MLA_OK) return st;
+    if (n_tokens < 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!x || !w_dkv || !w_kr || !seq_idx || !pos) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_dkv) || !aligned16(w_kr)) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int W = cfg->d_latent + cfg->d_rope;
+    if (tc_gemm_append_supported(cfg, n_tokens) && !g_tune[MLA_TUNE_FORCE_SIMT].load())
+        return tc_gemm_append(cfg, cache, x, w_dkv, w_kr, seq_idx, pos, n_tokens, s);
+    SimtGemmArgs g{};
+    g.A = x; g.lda = cfg->d_model; g.a_batch = 0;
+    g.B = w_dkv; g.ldb_k = cfg->d_latent; g.ldb_n = 1; g.b_batch = 0;
+    g.B2 = w_kr; g.ldb2_k = cfg->d_rope; g.n_split = cfg->d_latent;
+    g.C = cache->pool;
+    g.M = n_tokens; g.N = W; g.K = cfg->d_model;
+    g.seq_idx = seq_idx; g.pos = pos;
+    g.page_table = cache->page_table; g.max_pages = cache->max_pages; g.batch = cache->batch;
+    g.page_size = cfg->page_size; g.num_pages = cache->num_pages; g.width = W;
+    g.d_rope = cfg->d_rope; g.rope_base = cfg->rope_base;
+    dim3 grid((W + 63) / 64, (n_tokens + 63) / 64, 1);
+    if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_APPEND><<<grid, 256, 0, s>>>(g);
+    else simt_gemm_kernel<float, EPI_APPEND><<<grid, 256, 0, s>>>(g);
+    count_launches(1);
+    return launch_status();
+}
+
+mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q_rope,
+                        const int32_t* pos, const void* w_uk, void* q_cat, int32_t n_tokens,
+                        mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!q_nope || !q_rope || !pos || !w_uk || !q_cat) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_cat))
+        return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int n_h = cfg->n_heads, d_h = cfg->d_nope, d_c = cfg->d_latent, d_r = cfg->d_rope;
+    const int W = d_c + d_r;
+    if (tc_gemm_absorb_supported(cfg, n_tokens) && !g_tune[MLA_TUNE_FORCE_SIMT].load()) {
+        st = tc_gemm_absorb(cfg, q_nope, w_uk, q_cat, n_tokens, s);
+        if (st != MLA_OK) return st;
+    } else {
+        SimtGemmArgs g{};
+        g.A = q_nope; g.lda = (long long)n_h * d_h; g.a_batch = d_h;
+        g.B = w_uk; g.ldb_k = 1; g.ldb_n = (long long)n_h * d_h; g.b_batch = d_h;  // B(j,c) = W_UK[c, h*d_h+j]
+        g.C = q_cat; g.ldc = (long long)n_h * W; g.c_batch = W;
+        g.M = n_tokens; g.N = d_c; g.K = d_h;
+        dim3 grid((d_c + 63) / 64, (n_tokens + 63) / 64, n_h);
+        if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
+        else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
+        count_launches(1);
+        if ((st = launch_status()) != MLA_OK) return st;
+    }
+    long long pairs = (long long)n_tokens * n_h * (d_r / 2);
+    int blocks = (int)((pairs + 255) / 256 < 4096 ? (pairs + 255) / 256 : 4096);
+    if (cfg->dtype == MLA_BF16)
+        rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, cfg->rope_base);
+    else
+        rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, cfg->rope_base);
+    count_launches(1);
+    return launch_status();
+}
+
+mla_status mla_decode(const mla_config* cfg, const mla_cache* cache, const void* q_cat,
+                      void* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+                      mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if ((st = check_cache(cfg, cache)) != MLA_OK) return st;
+    if (!cache->seq_lens) return MLA_ERR_INVALID_ARG;
+    QuerySet qs{};
+    qs.mode = 0;
+    qs.n_queries = cache->batch;
+    qs.seq_lens = cache->seq_lens;
+    qs.page_size = cfg->page_size;
+    qs.max_len = cache->max_pages * cfg->page_size;
+    return attention(cfg, cache, qs, q_cat, o_lat, lse, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, int32_t seq,
+                       int32_t q_start, int32_t n_queries, const void* q_cat, void* o_lat,
+                       float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if ((st = check_cache(cfg, cache)) != MLA_OK) return st;
+    if (seq < 0 || seq >= cache->batch || q_start < 0 || n_queries < 0) return MLA_ERR_INVALID_ARG;
+    if ((long long)q_start + n_queries > (long long)cache->max_pages * cfg->page_size)
+        return MLA_ERR_INVALID_ARG;
+    QuerySet qs{};
+    qs.mode = 1;
+    qs.n_queries = n_queries;
+    qs.seq = seq;
+    qs.q_start = q_start;
+    qs.page_size = cfg->page_size;
+    qs.max_len = cache->max_pages * cfg->page_size;
+    return attention(cfg, cache, qs, q_cat, o_lat, lse, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, void* o,
+                   int32_t n_tokens, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!o_lat || !w_uv || !o || !aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o))
+        return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int n_h = cfg->n_heads, d_h = cfg->d_nope, d_c = cfg->d_latent;
+    if (tc_gemm_out_supported(cfg, n_tokens) && !g_tune[MLA_TUNE_FORCE_SIMT].load())
+        return tc_gemm_out(cfg, o_lat, w_uv, o, n_tokens, s);
+    SimtGemmArgs g{};
+    g.A = o_lat; g.lda = (long long)n_h * d_c; g.a_batch = d_c;
+    g.B = w_uv; g.ldb_k = (long long)n_h * d_h; g.ldb_n = 1; g.b_batch = d_h;   // B(c,j) = W_UV[c, h*d_h+j]
+    g.C = o; g.ldc = (long long)n_h * d_h; g.c_batch = d_h;
+    g.M = n_tokens; g.N = d_h; g.K = d_c;
+    dim3 grid((d_h + 63) / 64, (n_tokens + 63) / 64, n_h);
+    if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    count_launches(1);
+    return launch_status();
+}
+
+mla_status mla_get_device_error(mla_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+    return (mla_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,200 @@
+// Portable SIMT split attention over the paged latent cache (any dimensions, fp32 or bf16).
+//
+// Grid (U units, ceil(n_h/HG) head groups), 256 threads.  Each CTA walks the segments of its
+// unit (see sched.cuh); for each block of TB tokens it stages the cached rows in shared
+// memory as fp32, forms the HG x TB scores, updates the running max / sum per head (online
+// softmax) and accumulates o[h, :] += p[h, t] * c_kv[t, :].
+#pragma once
+
+#include "sched.cuh"
+
+namespace mla {
+
+struct AttnArgs {
+    QuerySet qs;
+    const void* q_cat;          // [Q, n_h, W]
+    const void* pool;           // [num_pages, P, W]
+    const int* page_table;      // [batch, max_pages]
+    int max_pages;
+    long long num_pages;
+    void* o_lat;                // [Q, n_h, d_c] final output (dtype)
+    float* lse;                 // [Q, n_h]
+    float* part_o;              // [2U, n_h, d_c] fp32 partials (o / l)
+    float* part_lse;            // [2U, n_h]
+    int n_units;
+    int n_h, d_c, width;
+    float scale;
+};
+
+constexpr int SIMT_TB = 32;     // tokens per staged block
+
+__host__ __device__ inline size_t simt_attn_smem_bytes(int hg, int width, int d_c) {
+    return sizeof(float) * ((size_t)hg * (width + 1) + (size_t)SIMT_TB * (width + 1) +
+                            (size_t)hg * SIMT_TB + (size_t)hg * d_c + 3 * (size_t)hg);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg) {
+    extern __shared__ float smem[];
+    __shared__ long long red[33];
+    const int W = a.width, Wp = W + 1, d_c = a.d_c;
+    float* q_s = smem;                           // [hg][Wp]
+    float* rows = q_s + (size_t)hg * Wp;         // [TB][Wp]
+    float* P = rows + (size_t)SIMT_TB * Wp;      // [hg][TB]
+    float* acc = P + (size_t)hg * SIMT_TB;       // [hg][d_c]
+    float* m_s = acc + (size_t)hg * d_c;         // [hg]
+    float* l_s = m_s + hg;                       // [hg]
+    float* alpha_s = l_s + hg;                   // [hg]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int h0 = blockIdx.y * hg;
+    const int nh_here = min(hg, a.n_h - h0);
+    const T* qc = reinterpret_cast<const T*>(a.q_cat);
+    const T* pool = reinterpret_cast<const T*>(a.pool);
+    const int ps = a.qs.page_size;
+
+    UnitCursor cur;
+    long long per;
+    cur.init(a.qs, blockIdx.x, a.n_units, red, &per);
+    Segment sg;
+    while (cur.next(a.qs, &sg)) {
+        // stage the queries of this head group, reset the running state
+        for (int e = tid; e < hg * W; e += blockDim.x) {
+            int h = e / W, k = e % W;
+            q_s[h * Wp + k] = h < nh_here ? to_f32(qc[((long long)sg.q * a.n_h + h0 + h) * W + k]) : 0.f;
+        }
+        for (int e = tid; e < hg * d_c; e += blockDim.x) acc[e] = 0.f;
+        for (int h = tid; h < hg; h += blockDim.x) { m_s[h] = -INFINITY; l_s[h] = 0.f; }
+        __syncthreads();
+
+        const int t_begin = sg.page_begin * ps;
+        const int t_end = min(sg.page_end * ps, sg.len);
+        for (int t0 = t_begin; t0 < t_end; t0 += SIMT_TB) {
+            // stage TB rows (token order), masking invalid pages
+            for (int e = tid; e < SIMT_TB * W; e += blockDim.x) {
+                int j = e / W, k = e % W, t = t0 + j;
+                float v = 0.f;
+                if (t < t_end) {
+                    int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + t / ps);
+                    if (page >= 0 && page < a.num_pages)
+                        v = to_f32(pool[((long long)page * ps + t % ps) * W + k]);
+                    else if (k == 0)
+                        set_device_error(MLA_ERR_DEVICE_BOUNDS);
+                }
+                rows[j * Wp + k] = v;
+            }
+            __syncthreads();
+            // scores
+            for (int e = tid; e < hg * SIMT_TB; e += blockDim.x) {
+                int h = e / SIMT_TB, j = e % SIMT_TB, t = t0 + j;
+                float s = -INFINITY;
+                if (h < nh_here && t < t_end) {
+                    const float* qr = q_s + h * Wp;
+                    const float* rr = rows + j * Wp;
+                    float d = 0.f;
+                    for (int k = 0; k < W; ++k) d = fmaf(qr[k], rr[k], d);
+                    s = d * a.scale;
+                }
+                P[h * SIMT_TB + j] = s;
+            }
+            __syncthreads();
+            // online softmax update, one warp per head
+            for (int h = warp; h < hg; h += nwarps) {
+                float s0 = P[h * SIMT_TB + lane];
+                float mx = warp_max(s0);
+                float m_old = m_s[h];
+                float m_new = fmaxf(m_old, mx);
+                float p0 = 0.f, alpha = 1.f;
+                if (m_new != -INFINITY) {
+                    p0 = (s0 == -INFINITY) ? 0.f : expf(s0 - m_new);
+                    alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+                }
+                float sum = warp_sum(p0);
+                P[h * SIMT_TB + lane] = p0;
+                if (lane == 0) {
+                    l_s[h] = l_s[h] * alpha + sum;
+                    m_s[h] = m_new;
+                    alpha_s[h] = alpha;
+                }
+            }
+            __syncthreads();
+            // o += p * c_kv
+            for (int e = tid; e < hg * d_c; e += blockDim.x) {
+                int h = e / d_c, c = e % d_c;
+                float v = acc[e] * alpha_s[h];
+                const float* ph = P + h * SIMT_TB;
+#pragma unroll 8
+                for (int j = 0; j < SIMT_TB; ++j) v = fmaf(ph[j], rows[j * Wp + c], v);
+                acc[e] = v;
+            }
+            __syncthreads();
+        }
+
+        // epilogue: final output or split partial
+        for (int e = tid; e < nh_here * d_c; e += blockDim.x) {
+            int h = e / d_c, c = e % d_c;
+            float l = l_s[h];
+            float v = l > 0.f ? acc[h * d_c + c] / l : 0.f;
+            if (sg.direct)
+                reinterpret_cast<T*>(a.o_lat)[((long long)sg.q * a.n_h + h0 + h) * d_c + c] = from_f32<T>(v);
+            else
+                a.part_o[((long long)sg.slot * a.n_h + h0 + h) * d_c + c] = v;
+        }
+        for (int h = tid; h < nh_here; h += blockDim.x) {
+            float l = l_s[h];
+            float L = l > 0.f ? m_s[h] + logf(l) : -INFINITY;
+            if (sg.direct) a.lse[(long long)sg.q * a.n_h + h0 + h] = L;
+            else a.part_lse[(long long)sg.slot * a.n_h + h0 + h] = L;
+        }
+        __syncthreads();
+    }
+}
+
+// Log-sum-exp merge of the split partials of every split query; also writes the empty-query
+// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h/8)), 256 threads: one warp per head.
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
+    __shared__ long long red[33];
+    const int q = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int h = blockIdx.y * 8 + warp;
+    const int d_c = a.d_c;
+    const int np = query_pages(a.qs, q);
+    long long total = block_total_pages(a.qs, red);
+    long long per = (total + a.n_units - 1) / a.n_units;
+    if (per < 1) per = 1;
+    long long pq = block_prefix_pages(a.qs, q, red);
+    if (h >= a.n_h) return;
+    T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * a.n_h + h) * d_c;
+    if (np == 0) {
+        for (int c = lane; c < d_c; c += 32) out[c] = from_f32<T>(0.f);
+        if (lane == 0) a.lse[(long long)q * a.n_h + h] = -INFINITY;
+        return;
+    }
+    const long long u_lo = pq / per, u_hi = (pq + np - 1) / per;
+    if (u_lo == u_hi) return;  // written directly by the attention kernel
+    float mx = -INFINITY;
+    for (long long u = u_lo; u <= u_hi; ++u) {
+        long long slot = (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1;
+        mx = fmaxf(mx, a.part_lse[slot * a.n_h + h]);
+    }
+    float wsum = 0.f;
+    for (long long u = u_lo; u <= u_hi; ++u) {
+        long long slot = (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1;
+        float l = a.part_lse[slot * a.n_h + h];
+        wsum += (l == -INFINITY) ? 0.f : expf(l - mx);
+    }
+    for (int c = lane; c < d_c; c += 32) {
+        float v = 0.f;
+        for (long long u = u_lo; u <= u_hi; ++u) {
+            long long slot = (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1;
+            float l = a.part_lse[slot * a.n_h + h];
+            float w = (l == -INFINITY) ? 0.f : expf(l - mx) / wsum;
+            v = fmaf(w, a.part_o[(slot * a.n_h + h) * d_c + c], v);
+        }
+        out[c] = from_f32<T>(v);
+    }
+    if (lane == 0) a.lse[(long long)q * a.n_h + h] = mx + logf(wsum);
+}
+
+}  // namespace mla

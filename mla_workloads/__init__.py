@@ -199,7 +199,7 @@ def make_decode_case(shape: Shape, dtype: str, lens, seed: int, *, spare_pages: 
     """A decode problem over a paged latent cache.
 
     Draw order (PCG64, `seed`): page table, cache rows per sequence, q_nope, q_rope,
-    W_UK, W_UV, W_O, then (append only) x, W_DKV, W_KR.
+    W_UK, W_UV, W_O, q_cat, then (append only) x, W_DKV, W_KR.
 
     With `append`, `lens` are the lengths BEFORE the append; one new token per sequence
     goes to position lens[b]; the returned `seq_lens` already include it.
@@ -223,6 +223,11 @@ def make_decode_case(shape: Shape, dtype: str, lens, seed: int, *, spare_pages: 
         w_uv=weight(rng, dc, H * dh, dtype),
         w_o=weight(rng, H * dh, shape.d_model, dtype),
     )
+    # synthetic absorbed queries for checking the attention kernel on its own: latent part
+    # N(0, d_h/d_c) (the spread of q_nope @ W_UK^T), RoPE part N(0, 1)
+    qc = normal(rng, (B, H, shape.width))
+    qc[..., :dc] *= np.float32(np.sqrt(dh / dc))
+    case["q_cat"] = quantise(qc, dtype)
     if append:
         case.update(
             x=quantise(normal(rng, (B, shape.d_model)), dtype),
@@ -302,3 +307,17 @@ def make_workload(name: str) -> dict:
 
 def replace_shape(shape: Shape, **kw) -> Shape:
     return dataclasses.replace(shape, **kw)
+
+
+def to_device(a: np.ndarray, dtype: str, device="cuda"):
+    """Copy a stored array to a torch device tensor of the storage type (bf16 bits -> bfloat16)."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def from_device(t) -> np.ndarray:
+    """Device tensor -> numpy float64 (bf16 widened exactly)."""
+    import torch
+    return t.detach().to("cpu", torch.float64).numpy()
