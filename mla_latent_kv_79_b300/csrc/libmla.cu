@@ -69,7 +69,7 @@ static mla_status check_config(const mla_config* c) {
     const size_t es = elem_size(c);
     if (((size_t)(c->d_latent + c->d_rope) * es) % 16 || ((size_t)c->d_latent * es) % 16)
         return MLA_ERR_UNSUPPORTED;
-    if (c->d_latent + c->d_rope > 1024 || c->d_latent > 1024) return MLA_ERR_UNSUPPORTED;
+    if (c->d_latent + c->d_rope > 1024 || c->d_latent > 1024 || c->d_rope > 1024) return MLA_ERR_UNSUPPORTED;
     return MLA_OK;
 }
 
@@ -157,7 +157,7 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
         count_launches(1);
         g_last_path = 1;
     }
-    dim3 cgrid(qs.n_queries, (n_h + 7) / 8);
+    dim3 cgrid(qs.n_queries, (n_h + 1) / 2);
     if (cfg->dtype == MLA_BF16) combine_kernel<bf16><<<cgrid, 256, 0, stream>>>(a);
     else combine_kernel<float><<<cgrid, 256, 0, stream>>>(a);
     count_launches(1);
@@ -271,8 +271,7 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
         count_launches(1);
         if ((st = launch_status()) != MLA_OK) return st;
     }
-    long long pairs = (long long)n_tokens * n_h * (d_r / 2);
-    int blocks = (int)((pairs + 255) / 256 < 4096 ? (pairs + 255) / 256 : 4096);
+    const int blocks = n_tokens;
     if (cfg->dtype == MLA_BF16)
         rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, cfg->rope_base);
     else

@@ -67,6 +67,9 @@ __device__ long long block_prefix_pages(const QuerySet& qs, int q, long long* re
     return block_sum_ll(s, red);
 }
 
+// Scratch for the block-wide helpers: red[0..32] reduction words, red[33..34] locate result.
+constexpr int SCHED_SCRATCH = 35;
+
 // First query q with P_{q+1} > flat, and the page offset of `flat` inside it.  Block-wide.
 // `flat` must be < total.
 __device__ void block_locate(const QuerySet& qs, long long flat, int* q_out, int* page_out, long long* red) {
@@ -84,7 +87,8 @@ __device__ void block_locate(const QuerySet& qs, long long flat, int* q_out, int
         return;
     }
     // decode: stream the lengths in chunks of blockDim with a running offset.
-    __shared__ int s_found_q, s_found_page;
+    long long& s_found_q = red[33];
+    long long& s_found_page = red[34];
     if (threadIdx.x == 0) { s_found_q = -1; s_found_page = 0; }
     long long run = 0;
     for (int c0 = 0; c0 < qs.n_queries; c0 += blockDim.x) {
@@ -115,8 +119,8 @@ __device__ void block_locate(const QuerySet& qs, long long flat, int* q_out, int
         if (s_found_q >= 0) break;  // uniform: read after the barrier
     }
     __syncthreads();
-    *q_out = s_found_q < 0 ? 0 : s_found_q;
-    *page_out = s_found_page;
+    *q_out = s_found_q < 0 ? 0 : (int)s_found_q;
+    *page_out = (int)s_found_page;
     __syncthreads();
 }
 

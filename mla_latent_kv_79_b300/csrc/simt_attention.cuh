@@ -36,7 +36,7 @@ __host__ __device__ inline size_t simt_attn_smem_bytes(int hg, int width, int d_
 template <typename T>
 __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg) {
     extern __shared__ float smem[];
-    __shared__ long long red[33];
+    __shared__ long long red[SCHED_SCRATCH];
     const int W = a.width, Wp = W + 1, d_c = a.d_c;
     float* q_s = smem;                           // [hg][Wp]
     float* rows = q_s + (size_t)hg * Wp;         // [TB][Wp]
@@ -151,50 +151,54 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
 }
 
 // Log-sum-exp merge of the split partials of every split query; also writes the empty-query
-// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h/8)), 256 threads: one warp per head.
+// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h / 2)), 256 threads: 128 threads per head,
+// each thread owns 4 consecutive latent columns (d_c <= 512) and merges them over the slots.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
-    __shared__ long long red[33];
+    __shared__ long long red[SCHED_SCRATCH];
     const int q = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int h = blockIdx.y * 8 + warp;
+    const int sub = threadIdx.x >> 7, t = threadIdx.x & 127;
+    const int h = blockIdx.y * 2 + sub;
     const int d_c = a.d_c;
     const int np = query_pages(a.qs, q);
-    long long total = block_total_pages(a.qs, red);
+    const long long total = block_total_pages(a.qs, red);
     long long per = (total + a.n_units - 1) / a.n_units;
     if (per < 1) per = 1;
-    long long pq = block_prefix_pages(a.qs, q, red);
+    const long long pq = block_prefix_pages(a.qs, q, red);
     if (h >= a.n_h) return;
     T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * a.n_h + h) * d_c;
     if (np == 0) {
-        for (int c = lane; c < d_c; c += 32) out[c] = from_f32<T>(0.f);
-        if (lane == 0) a.lse[(long long)q * a.n_h + h] = -INFINITY;
+        for (int c = t; c < d_c; c += 128) out[c] = from_f32<T>(0.f);
+        if (t == 0) a.lse[(long long)q * a.n_h + h] = -INFINITY;
         return;
     }
     const long long u_lo = pq / per, u_hi = (pq + np - 1) / per;
     if (u_lo == u_hi) return;  // written directly by the attention kernel
+    auto slot_of = [&](long long u) { return (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1; };
     float mx = -INFINITY;
-    for (long long u = u_lo; u <= u_hi; ++u) {
-        long long slot = (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1;
-        mx = fmaxf(mx, a.part_lse[slot * a.n_h + h]);
-    }
+    for (long long u = u_lo; u <= u_hi; ++u) mx = fmaxf(mx, a.part_lse[slot_of(u) * a.n_h + h]);
     float wsum = 0.f;
     for (long long u = u_lo; u <= u_hi; ++u) {
-        long long slot = (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1;
-        float l = a.part_lse[slot * a.n_h + h];
-        wsum += (l == -INFINITY) ? 0.f : expf(l - mx);
+        const float l = a.part_lse[slot_of(u) * a.n_h + h];
+        wsum += (l == -INFINITY) ? 0.f : __expf(l - mx);
     }
-    for (int c = lane; c < d_c; c += 32) {
-        float v = 0.f;
+    const float inv = 1.f / wsum;
+    for (int c = 4 * t; c < d_c; c += 512) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (long long u = u_lo; u <= u_hi; ++u) {
-            long long slot = (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1;
-            float l = a.part_lse[slot * a.n_h + h];
-            float w = (l == -INFINITY) ? 0.f : expf(l - mx) / wsum;
-            v = fmaf(w, a.part_o[(slot * a.n_h + h) * d_c + c], v);
+            const long long sl = slot_of(u);
+            const float l = a.part_lse[sl * a.n_h + h];
+            const float w = (l == -INFINITY) ? 0.f : __expf(l - mx) * inv;
+            const float4 v = *reinterpret_cast<const float4*>(a.part_o + (sl * a.n_h + h) * d_c + c);
+            acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
         }
-        out[c] = from_f32<T>(v);
+        out[c] = from_f32<T>(acc.x);
+        if (c + 1 < d_c) out[c + 1] = from_f32<T>(acc.y);
+        if (c + 2 < d_c) out[c + 2] = from_f32<T>(acc.z);
+        if (c + 3 < d_c) out[c + 3] = from_f32<T>(acc.w);
     }
-    if (lane == 0) a.lse[(long long)q * a.n_h + h] = mx + logf(wsum);
+    if (t == 0) a.lse[(long long)q * a.n_h + h] = mx + logf(wsum);
 }
 
 }  // namespace mla

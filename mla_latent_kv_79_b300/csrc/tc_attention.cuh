@@ -1,15 +1,542 @@
-// tcgen05 (sm_103a) kernels: declarations of the fast-path dispatch.  The kernels follow.
+// tcgen05 split attention over the paged latent cache (sm_103a fast path).
+//
+// Shapes: n_h = 128 heads, d_c = 512, d_r = 64 (W = 576), page = 64 tokens, bf16 operands,
+// fp32 softmax and accumulation.  This is the absorbed decode of the MLA glossary page (the
+// up-projection folded into the query and the output) over the latent cache of the
+// operator-notes page, section 3: all heads attend to the same cached row [c_kv | k_rope].
+//
+// One unit of the split schedule (sched.cuh) runs on a cluster of two CTAs with different
+// jobs, because one SM's 512 TMEM columns cannot hold both the query (288 columns of bf16
+// pairs) and the 128 x 512 fp32 output accumulator:
+//
+//   score CTA (rank 0)  TMEM: Q [0,288), S double buffer [288,416)
+//     S = Q . page^T over all 576 columns, online softmax (running max raised only when it
+//     grows by more than 2^8: O and l share the stale max, so the result is exact), then
+//     P (bf16, 16 KB) plus (alpha, l) per head are stored with st.async straight into the
+//     value CTA's shared memory, completing bytes on its mbarrier.
+//   value CTA (rank 1)  TMEM: O [0,512)
+//     rescales O rows when alpha != 1, then O += P . page[:, 0:512] with P as the
+//     shared-memory A operand; drains O / l at the end of every segment.
+//
+// Each page is read from HBM once: its eight 64-column latent chunks are TMA-multicast to
+// both CTAs (each CTA issues four), the RoPE chunk goes to the score CTA only.  A stage is
+// refilled when both CTAs have released it (commits multicast to both empty barriers).  The
+// score-to-value traffic is one-directional, so neither CTA waits on a round trip.
+//
+// Roles (192 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
+// (one TMEM lane quarter each, one head per thread) softmax in the score CTA, rescale and
+// drain in the value CTA.  Every wait is bounded.
 #pragma once
+
+#include <cudaTypedefs.h>
 
 #include "sched.cuh"
 #include "simt_attention.cuh"
+#include "tc_ptx.cuh"
 
 namespace mla {
+namespace tca {
 
-inline bool tc_attention_supported(const mla_config*, const mla_cache*, int, int) { return false; }
-inline mla_status tc_attention_launch(const AttnArgs&, const mla_cache*, unsigned long long, cudaStream_t) {
-    return MLA_ERR_UNSUPPORTED;
+constexpr int NH = 128, DC = 512, DR = 64, WID = 576, PAGE = 64;
+constexpr int CHUNK = 64 * 128;                   // 64 rows x 64 bf16, 128-byte swizzled
+constexpr int LAT_CHUNKS = 8;
+constexpr int STAGE_BYTES = LAT_CHUNKS * CHUNK;   // 64 KB latent part of a page
+constexpr int STAGES = 3;
+constexpr int OFF_R = STAGES * STAGE_BYTES;       // score CTA: RoPE chunks; value CTA: P buffers
+constexpr int P_BYTES = NH * 128;                 // P [128 heads x 64 tokens] bf16, SW128 K-major
+constexpr int META_BYTES = NH * 8;                // (alpha, l) per head, fp32
+constexpr int PBUF_BYTES = P_BYTES + META_BYTES;
+constexpr int R_BYTES = 2 * PBUF_BYTES;
+static_assert(R_BYTES >= STAGES * CHUNK, "RoPE stages must fit the shared region");
+constexpr int OFF_BARS = OFF_R + R_BYTES;
+enum {
+    B_FULL = 0,                  // [STAGES] page landed (own expect_tx + bytes from both issuers)
+    B_EMPTY = B_FULL + STAGES,   // [STAGES] both CTAs released the stage (2 commits)
+    B_SFULL = B_EMPTY + STAGES,  // [2] score CTA: S buffer written
+    B_SFREE = B_SFULL + 2,       // [2] score CTA: S buffer read by the 4 softmax warps
+    B_QFULL = B_SFREE + 2,       // score CTA: Q of the segment in TMEM
+    B_PFULL = B_QFULL + 1,       // [2] value CTA: P + meta landed (own expect_tx + bytes)
+    B_PEMPTY = B_PFULL + 2,      // [2] score CTA: value CTA's PV finished with P buffer b
+    B_PREADY = B_PEMPTY + 2,     // [2] value CTA: O rescaled, P buffer b ready for the MMA
+    B_PVDONE = B_PREADY + 2,     // [2] value CTA: PV of the page that used P buffer b complete
+    B_OFREE = B_PVDONE + 2,      // value CTA: O drained
+    B_DONE = B_OFREE + 1,        // MMA drain at exit
+    NBARS
+};
+constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+constexpr int OFF_RED = OFF_MISC + 16;            // schedule scratch (SCHED_SCRATCH words)
+constexpr int SMEM_BYTES = OFF_RED + SCHED_SCRATCH * 8;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int TM_Q = 0, TM_S = 288, TM_O = 0;
+constexpr int NTHREADS = 192;
+constexpr float TAU = 8.0f;  // log2 units
+constexpr float LN2 = 0.6931471805599453f;
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 64, false, false);
+constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, 256, false, true);
+
+struct TcArgs {
+    AttnArgs a;
+    unsigned long long wait_ns;
+    float scale_log2;
+};
+
+struct WaitCtl {
+    unsigned long long limit_ns;
+    volatile int* abort;
+    bool ignore_abort;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& w, bool cluster_scope = false) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            if (!w.ignore_abort && *w.abort) return false;
+            const unsigned long long t = globaltimer_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > w.limit_ns) {
+                *w.abort = 1;
+                set_device_error(MLA_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
 }
+
+// Warp-uniform bounded wait: every lane observes the phase (acquire), all lanes leave together.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, bool cluster_scope,
+                                          int lane) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        const bool ok = cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if ((i & 63u) == 63u) {
+            int stop = 0;
+            if (lane == 0) {
+                if (*w.abort) stop = 1;
+                const unsigned long long t = globaltimer_ns();
+                if (t0 == 0) t0 = t;
+                else if (t - t0 > w.limit_ns) {
+                    *w.abort = 1;
+                    set_device_error(MLA_ERR_DEVICE_TIMEOUT);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + OFF_BARS + 8u * (uint32_t)i; }
+
+// ----------------------------------------------------------------------------- warp 0: TMA
+// Both CTAs run the same page sequence; rank 0 issues latent chunks 0-3 (multicast) and the
+// RoPE chunk (local), rank 1 issues latent chunks 4-7 (multicast).
+__device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tm, UnitCursor c, uint32_t base,
+                                         uint32_t rank, const WaitCtl& wc) {
+    uint32_t g = 0;
+    bool ok = true;
+    Segment sg;
+    const uint32_t expect = rank == 0 ? (uint32_t)(STAGE_BYTES + CHUNK) : (uint32_t)STAGE_BYTES;
+    const int c0 = rank == 0 ? 0 : 4;
+    while (ok && c.next(a.qs, &sg)) {
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+            const uint32_t stage = g % STAGES;
+            if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
+            int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + pg);
+            if (page < 0 || page >= a.num_pages) {
+                set_device_error(MLA_ERR_DEVICE_BOUNDS);
+                page = 0;  // keep the pipeline fed; the result of this query is void
+            }
+            const uint32_t fb = bar_addr(base, B_FULL + stage);
+            ptx::mbar_arrive_expect_tx(fb, expect);
+            const uint32_t dst = base + stage * STAGE_BYTES;
+            for (int cc = c0; cc < c0 + 4; ++cc)
+                ptx::tma_load_2d_mc(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb, (uint16_t)0x3);
+            if (rank == 0) ptx::tma_load_2d(base + OFF_R + stage * CHUNK, tm, DC, page * PAGE, fb);
+        }
+    }
+    if (!ok) {  // let loads already in flight land before the CTA leaves
+        WaitCtl w2 = wc;
+        w2.ignore_abort = true;
+        w2.limit_ns = 20000000ull;
+        for (uint32_t k = g > (uint32_t)STAGES ? g - STAGES : 0u; k < g; ++k)
+            wait_bar(bar_addr(base, B_FULL + k % STAGES), (k / STAGES) & 1u, w2);
+    }
+}
+
+// ----------------------------------------------------------------------------- score CTA
+__device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
+                                          const WaitCtl& wc) {
+    uint32_t g = 0, segn = 0;
+    bool ok = true;
+    Segment sg;
+    while (ok && c.next(a.qs, &sg)) {
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+            const uint32_t stage = g % STAGES, sb = g & 1u;
+            if (!wait_bar(bar_addr(base, B_FULL + stage), (g / STAGES) & 1u, wc)) { ok = false; break; }
+            if (pg == sg.page_begin && !wait_bar(bar_addr(base, B_QFULL), segn & 1u, wc)) { ok = false; break; }
+            if (!wait_bar(bar_addr(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t st = base + stage * STAGE_BYTES;
+            const uint32_t d = tmem + TM_S + sb * 64;
+            for (int cc = 0; cc < 9; ++cc) {
+                const uint32_t cb = cc < LAT_CHUNKS ? st + cc * CHUNK : base + OFF_R + stage * CHUNK;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA, 4 per 64-column chunk
+                    ptx::mma_ts(d, tmem + TM_Q + cc * 32 + kk * 8, ptx::desc_sw128(cb + kk * 32, 16, 1024), IDESC_QK,
+                                (cc | kk) ? 1u : 0u);
+            }
+            ptx::tc_commit(bar_addr(base, B_SFULL + sb));
+            ptx::tc_commit_mc(bar_addr(base, B_EMPTY + stage), (uint16_t)0x3);
+        }
+        ++segn;
+    }
+    ptx::tc_commit(bar_addr(base, B_DONE));
+    WaitCtl w2 = wc;
+    w2.ignore_abort = true;
+    wait_bar(bar_addr(base, B_DONE), 0, w2);
+}
+
+__device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, uint32_t base, uint32_t tmem,
+                                              uint32_t peer, int warp, int lane, const WaitCtl& wc) {
+    const AttnArgs& a = args.a;
+    const int qd = warp & 3;  // TMEM lane quarter this warp may access
+    const int h = qd * 32 + lane;
+    const uint32_t lb = (uint32_t)(qd * 32) << 16;
+    const uint32_t tQ = tmem + lb + TM_Q, tS = tmem + lb + TM_S;
+    const uint32_t pbuf_r = ptx::mapa(base + OFF_R, peer);          // value CTA's P buffers
+    const uint32_t pfull_r = ptx::mapa(bar_addr(base, B_PFULL), peer);
+    const uint32_t sw = (uint32_t)(h & 7);
+    const bf16* qc = reinterpret_cast<const bf16*>(a.q_cat);
+    uint32_t g = 0;
+    bool ok = true;
+    Segment sg;
+    while (ok && c.next(a.qs, &sg)) {
+        // this segment's query row into TMEM; the previous segment's QK MMAs are complete
+        // because their S was consumed
+        const uint4* qrow = reinterpret_cast<const uint4*>(qc + ((size_t)sg.q * NH + h) * WID);
+        for (int cc = 0; cc < 9; ++cc) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 v = __ldg(qrow + cc * 8 + i);
+                r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+            }
+            ptx::tmem_st32(tQ + cc * 32, r);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_QFULL));
+
+        float m_run = -INFINITY, l = 0.f;
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+            const uint32_t sb = g & 1u, use = g >> 1;
+            if (!warp_wait(bar_addr(base, B_SFULL + sb), use & 1u, wc, false, lane)) { ok = false; break; }
+            ptx::tc_fence_after();
+            float s[64];
+            {
+                uint32_t r[32];
+                ptx::tmem_ld32(tS + sb * 64, r);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
+                ptx::tmem_ld32(tS + sb * 64 + 32, r);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_SFREE + sb));
+
+            // scaled scores in log2 units; tokens past the sequence end are masked
+            const int valid = sg.len - pg * PAGE;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float x = j < valid ? s[j] * args.scale_log2 : -INFINITY;
+                s[j] = x;
+                mx = fmaxf(mx, x);
+            }
+            float alpha = 1.f;
+            if (mx > m_run + TAU) {
+                alpha = ptx::ex2(m_run - mx);
+                m_run = mx;
+                l *= alpha;
+            }
+            float sum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = ptx::ex2(s[2 * j] - m_run), p1 = ptx::ex2(s[2 * j + 1] - m_run);
+                sum += p0 + p1;
+                pk[j] = ptx::pack_bf16(p0, p1);
+            }
+            l += sum;
+            // P row h -> value CTA, 128-byte swizzled (16-byte chunk k at k ^ (h & 7))
+            const uint32_t pb = g & 1u;
+            if (!warp_wait(bar_addr(base, B_PEMPTY + pb), (use & 1u) ^ 1u, wc, true, lane)) { ok = false; break; }
+            const uint32_t row = pbuf_r + pb * PBUF_BYTES + (uint32_t)h * 128u;
+            const uint32_t fb = pfull_r + 8u * pb;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                ptx::st_async_v4_b32(row + ((k ^ sw) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3], fb);
+            ptx::st_async_v2_f32(pbuf_r + pb * PBUF_BYTES + P_BYTES + (uint32_t)h * 8u, alpha, l, fb);
+        }
+        if (!ok) break;
+        const float lse = l > 0.f ? (m_run + __log2f(l)) * LN2 : -INFINITY;
+        if (sg.direct) a.lse[(size_t)sg.q * NH + h] = lse;
+        else a.part_lse[(size_t)sg.slot * NH + h] = lse;
+    }
+}
+
+// ----------------------------------------------------------------------------- value CTA
+__device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
+                                          const WaitCtl& wc) {
+    uint32_t g = 0, segn = 0;
+    bool ok = true;
+    Segment sg;
+    while (ok && c.next(a.qs, &sg)) {
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+            const bool first = pg == sg.page_begin;
+            const uint32_t stage = g % STAGES, pb = g & 1u;
+            if (!wait_bar(bar_addr(base, B_FULL + stage), (g / STAGES) & 1u, wc)) { ok = false; break; }
+            if (!wait_bar(bar_addr(base, B_PREADY + pb), (g >> 1) & 1u, wc)) { ok = false; break; }
+            if (first && segn > 0 && !wait_bar(bar_addr(base, B_OFREE), (segn - 1) & 1u, wc)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t st = base + stage * STAGE_BYTES;
+            const uint32_t pa = base + OFF_R + pb * PBUF_BYTES;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // 16 tokens per MMA; V is MN-major: chunks 8 KB apart
+                    ptx::mma_ss(tmem + TM_O + hf * 256, ptx::desc_sw128(pa + kk * 32, 16, 1024),
+                                ptx::desc_sw128(st + hf * 4 * CHUNK + kk * 2048, CHUNK, 1024), IDESC_PV,
+                                (first && kk == 0) ? 0u : 1u);
+            }
+            ptx::tc_commit(bar_addr(base, B_PVDONE + pb));
+            ptx::tc_commit_mc(bar_addr(base, B_EMPTY + stage), (uint16_t)0x3);
+            ptx::tc_commit_mc(bar_addr(base, B_PEMPTY + pb), (uint16_t)0x1);
+        }
+        ++segn;
+    }
+    ptx::tc_commit(bar_addr(base, B_DONE));
+    WaitCtl w2 = wc;
+    w2.ignore_abort = true;
+    wait_bar(bar_addr(base, B_DONE), 0, w2);
+}
+
+__device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem, int warp,
+                                            int lane, const WaitCtl& wc) {
+    const int qd = warp & 3;
+    const int h = qd * 32 + lane;
+    const uint32_t tO = tmem + ((uint32_t)(qd * 32) << 16) + TM_O;
+    uint32_t g = 0;
+    bool ok = true;
+    Segment sg;
+    while (ok && c.next(a.qs, &sg)) {
+        float l_last = 0.f;
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+            const bool first = pg == sg.page_begin;
+            const uint32_t pb = g & 1u, use = g >> 1;
+            if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(bar_addr(base, B_PFULL + pb), PBUF_BYTES);
+            if (!warp_wait(bar_addr(base, B_PFULL + pb), use & 1u, wc, true, lane)) { ok = false; break; }
+            const float2 meta = ptx::ld_shared_v2(base + OFF_R + pb * PBUF_BYTES + P_BYTES + (uint32_t)h * 8u);
+            l_last = meta.y;
+            const bool resc = !first && meta.x != 1.f;
+            if (__any_sync(0xffffffffu, resc)) {
+                // O must be stable: the previous page's PV has completed.  pvdone is kept per P
+                // buffer so that no parity wait here is ever two phases away from its target.
+                const uint32_t gp = g - 1;
+                if (!warp_wait(bar_addr(base, B_PVDONE + (gp & 1u)), (gp >> 1) & 1u, wc, false, lane)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const float alpha = resc ? meta.x : 1.f;
+                for (int k = 0; k < 16; ++k) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(tO + 32 * k, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                    ptx::tmem_st32(tO + 32 * k, r);
+                }
+                ptx::tmem_wait_st();
+            }
+            ptx::fence_proxy_async();  // P arrived through the generic proxy; the MMA reads it via the async proxy
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_PREADY + pb));
+        }
+        if (!ok) break;
+        // drain O / l once the segment's last PV has completed
+        {
+            const uint32_t gl = g - 1;
+            if (!warp_wait(bar_addr(base, B_PVDONE + (gl & 1u)), (gl >> 1) & 1u, wc, false, lane)) { ok = false; break; }
+        }
+        ptx::tc_fence_after();
+        const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
+        for (int k = 0; k < 16; ++k) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tO + 32 * k, r);
+            ptx::tmem_wait_ld();
+            if (sg.direct) {
+                uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(a.o_lat) + ((size_t)sg.q * NH + h) * DC +
+                                                     32 * k);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint4 v;
+                    v.x = ptx::pack_bf16(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+                    v.y = ptx::pack_bf16(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+                    v.z = ptx::pack_bf16(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+                    v.w = ptx::pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+                    d4[i] = v;
+                }
+            } else {
+                float4* d4 = reinterpret_cast<float4*>(a.part_o + ((size_t)sg.slot * NH + h) * DC + 32 * k);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                        __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+            }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_OFREE));
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    tc_attention_kernel(const __grid_constant__ CUtensorMap tmap, const TcArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const AttnArgs& a = args.a;
+    const uint32_t base = ptx::smem_u32(smem);
+    if (base & 1023u) {  // both CTAs share the layout, so both leave here together
+        if (threadIdx.x == 0) set_device_error(MLA_ERR_UNSUPPORTED);
+        return;
+    }
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    long long* red = reinterpret_cast<long long*>(smem + OFF_RED);
+
+    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const int unit = blockIdx.x >> 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(bar_addr(base, B_FULL + s), 1);
+            ptx::mbar_init(bar_addr(base, B_EMPTY + s), 2);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_addr(base, B_SFULL + b), 1);
+            ptx::mbar_init(bar_addr(base, B_SFREE + b), 4);
+            ptx::mbar_init(bar_addr(base, B_PFULL + b), 1);
+            ptx::mbar_init(bar_addr(base, B_PEMPTY + b), 1);
+            ptx::mbar_init(bar_addr(base, B_PREADY + b), 4);
+            ptx::mbar_init(bar_addr(base, B_PVDONE + b), 1);
+        }
+        ptx::mbar_init(bar_addr(base, B_QFULL), 4);
+        ptx::mbar_init(bar_addr(base, B_OFREE), 4);
+        ptx::mbar_init(bar_addr(base, B_DONE), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) ptx::prefetch_tmap(&tmap);
+    if (warp == 1) {
+        ptx::tmem_alloc(base + OFF_MISC, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
+    const uint32_t tmem = *tmem_slot;
+
+    UnitCursor cur;
+    long long per;
+    cur.init(a.qs, unit, a.n_units, red, &per);
+    const WaitCtl wc{args.wait_ns, abort_flag, false};
+
+    if (warp == 0) {
+        if (lane == 0) producer(a, &tmap, cur, base, rank, wc);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (rank == 0) score_mma(a, cur, base, tmem, wc);
+            else value_mma(a, cur, base, tmem, wc);
+        }
+    } else if (rank == 0) {
+        score_softmax(args, cur, base, tmem, peer, warp, lane, wc);
+    } else {
+        value_warps(a, cur, base, tmem, warp, lane, wc);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {  // give copies that a peer may still have in flight time to land
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) {
+        }
+    }
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+    ptx::cluster_sync();  // no CTA leaves while its peer may still write into it
+}
+
+// ----------------------------------------------------------------------------- host side
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D map over the pool viewed as [num_pages*64 rows, 576 columns] bf16; box 64 x 64, 128B swizzle.
+inline bool encode_pool_map(CUtensorMap* tm, void* pool, long long num_pages) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)WID, (cuuint64_t)num_pages * PAGE};
+    cuuint64_t strides[1] = {(cuuint64_t)WID * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tca
+
+inline bool tc_attention_supported(const mla_config* c, const mla_cache* k, int cc_major, int cc_minor) {
+    return c->dtype == MLA_BF16 && c->n_heads == tca::NH && c->d_latent == tca::DC && c->d_rope == tca::DR &&
+           c->page_size == tca::PAGE && cc_major == 10 && cc_minor == 3 && k->num_pages * tca::PAGE < (1LL << 31);
+}
+
+inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache, unsigned long long wait_ns,
+                                      cudaStream_t stream) {
+    CUtensorMap tm;
+    if (!tca::encode_pool_map(&tm, cache->pool, cache->num_pages)) return MLA_ERR_CUDA;
+    tca::TcArgs t;
+    t.a = a;
+    t.wait_ns = wait_ns;
+    t.scale_log2 = a.scale * 1.4426950408889634f;
+    if (cudaFuncSetAttribute(tca::tc_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tca::SMEM_BYTES) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    tca::tc_attention_kernel<<<2 * a.n_units, tca::NTHREADS, tca::SMEM_BYTES, stream>>>(tm, t);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 inline bool tc_gemm_append_supported(const mla_config*, int) { return false; }
 inline mla_status tc_gemm_append(const mla_config*, const mla_cache*, const void*, const void*, const void*,
                                  const int32_t*, const int32_t*, int32_t, cudaStream_t) {

@@ -13,10 +13,21 @@ TOL_LSE_BF16 = 1e-3
 # fp32 path: fp32 accumulation over at most a few thousand terms.
 TOL_OUT_F32 = 1e-4
 TOL_LSE_F32 = 1e-4
-# Chains that round an intermediate (q_cat) to bf16 before the attention kernel: the score
-# error of a bf16-rounded query is ~ scale * 2^-8/sqrt(3) * ||q . k||_2 ~ 1.1e-3 per score at
-# the DeepSeek-V2 shapes, so lse may move by a few of those when one token dominates.
-TOL_LSE_BF16_CHAIN = 5e-3
+BF16_U = 2.0 ** -8   # unit roundoff of bf16 (8 significant bits, round to nearest)
+
+
+def lse_rounding_bound(q, keys, appended=(), scale=1.0):
+    """Rigorous first-order bound on |lse' - lse| when the query q and the cache rows listed
+    in `appended` are rounded to bf16 before attention (every other row is already bf16).
+
+    lse is 1-Lipschitz in the max-norm of the scores, and a score q.k moves by at most
+    scale * sum_c (u |q_c||k_c|  +  [k rounded] (u + u^2) |q_c||k_c|).
+    q [n_h, W], keys [L, W] (float64 oracle values).  Returns [n_h]."""
+    a = np.abs(q) @ np.abs(keys).T                     # [n_h, L]
+    per = np.full(keys.shape[0], BF16_U)
+    for t in appended:
+        per[t] += BF16_U + BF16_U * BF16_U
+    return scale * np.max(a * per[None, :], axis=1)
 
 
 def rel(g, r) -> float:
