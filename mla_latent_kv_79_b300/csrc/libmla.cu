@@ -14,6 +14,7 @@
 #include "simt_gemm.cuh"
 #include "simt_attention.cuh"
 #include "tc_attention.cuh"
+#include "tc_gemm.cuh"
 
 namespace mla {
 
@@ -157,9 +158,9 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
         count_launches(1);
         g_last_path = 1;
     }
-    dim3 cgrid(qs.n_queries, (n_h + 1) / 2);
-    if (cfg->dtype == MLA_BF16) combine_kernel<bf16><<<cgrid, 256, 0, stream>>>(a);
-    else combine_kernel<float><<<cgrid, 256, 0, stream>>>(a);
+    dim3 cgrid(qs.n_queries, (d_c / 4 + COMBINE_QUADS - 1) / COMBINE_QUADS);
+    if (cfg->dtype == MLA_BF16) combine_kernel<bf16><<<cgrid, 128, 0, stream>>>(a);
+    else combine_kernel<float><<<cgrid, 128, 0, stream>>>(a);
     count_launches(1);
     return launch_status();
 }
@@ -256,9 +257,13 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int n_h = cfg->n_heads, d_h = cfg->d_nope, d_c = cfg->d_latent, d_r = cfg->d_rope;
     const int W = d_c + d_r;
-    if (tc_gemm_absorb_supported(cfg, n_tokens) && !g_tune[MLA_TUNE_FORCE_SIMT].load()) {
-        st = tc_gemm_absorb(cfg, q_nope, w_uk, q_cat, n_tokens, s);
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    const unsigned long long wait_ns = (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull;
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_absorb_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
+        st = tc_gemm_absorb(cfg, q_nope, w_uk, q_cat, n_tokens, wait_ns, s);
         if (st != MLA_OK) return st;
+        count_launches(1);
     } else {
         SimtGemmArgs g{};
         g.A = q_nope; g.lda = (long long)n_h * d_h; g.a_batch = d_h;
@@ -271,7 +276,7 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
         count_launches(1);
         if ((st = launch_status()) != MLA_OK) return st;
     }
-    const int blocks = n_tokens;
+    const dim3 blocks(n_tokens, (n_h + ROPE_HEADS - 1) / ROPE_HEADS);
     if (cfg->dtype == MLA_BF16)
         rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, cfg->rope_base);
     else
@@ -327,8 +332,14 @@ mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, v
         return MLA_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int n_h = cfg->n_heads, d_h = cfg->d_nope, d_c = cfg->d_latent;
-    if (tc_gemm_out_supported(cfg, n_tokens) && !g_tune[MLA_TUNE_FORCE_SIMT].load())
-        return tc_gemm_out(cfg, o_lat, w_uv, o, n_tokens, s);
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_out_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
+        st = tc_gemm_out(cfg, o_lat, w_uv, o, n_tokens,
+                         (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull, s);
+        if (st == MLA_OK) count_launches(1);
+        return st;
+    }
     SimtGemmArgs g{};
     g.A = o_lat; g.lda = (long long)n_h * d_c; g.a_batch = d_c;
     g.B = w_uv; g.ldb_k = (long long)n_h * d_h; g.ldb_n = 1; g.b_batch = d_h;   // B(c,j) = W_UV[c, h*d_h+j]

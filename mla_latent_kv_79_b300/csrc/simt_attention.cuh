@@ -19,7 +19,7 @@ struct AttnArgs {
     long long num_pages;
     void* o_lat;                // [Q, n_h, d_c] final output (dtype)
     float* lse;                 // [Q, n_h]
-    float* part_o;              // [2U, n_h, d_c] fp32 partials (o / l)
+    float* part_o;              // [2U, d_c/4, n_h, 4] fp32 partials (o / l), see part_index
     float* part_lse;            // [2U, n_h]
     int n_units;
     int n_h, d_c, width;
@@ -27,6 +27,12 @@ struct AttnArgs {
 };
 
 constexpr int SIMT_TB = 32;     // tokens per staged block
+
+// Split partials are stored head-contiguous per column quad, [slot][c/4][h][c%4], so that a
+// warp of consecutive heads writes (and the combine reads) contiguous memory.
+__device__ __forceinline__ size_t part_index(long long slot, int h, int c, int n_h, int d_c) {
+    return (((size_t)slot * (d_c / 4) + (c >> 2)) * n_h + h) * 4 + (c & 3);
+}
 
 __host__ __device__ inline size_t simt_attn_smem_bytes(int hg, int width, int d_c) {
     return sizeof(float) * ((size_t)hg * (width + 1) + (size_t)SIMT_TB * (width + 1) +
@@ -138,7 +144,7 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
             if (sg.direct)
                 reinterpret_cast<T*>(a.o_lat)[((long long)sg.q * a.n_h + h0 + h) * d_c + c] = from_f32<T>(v);
             else
-                a.part_o[((long long)sg.slot * a.n_h + h0 + h) * d_c + c] = v;
+                a.part_o[part_index(sg.slot, h0 + h, c, a.n_h, d_c)] = v;
         }
         for (int h = tid; h < nh_here; h += blockDim.x) {
             float l = l_s[h];
@@ -151,54 +157,72 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
 }
 
 // Log-sum-exp merge of the split partials of every split query; also writes the empty-query
-// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h / 2)), 256 threads: 128 threads per head,
-// each thread owns 4 consecutive latent columns (d_c <= 512) and merges them over the slots.
+// result (o = 0, lse = -inf).  Grid (Q, ceil(d_c / 32)), 128 threads: a thread per head (loop
+// when n_h > 128), eight column quads per block, partial reads coalesced across heads.
+constexpr int COMBINE_QUADS = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(128) combine_kernel(AttnArgs a) {
     __shared__ long long red[SCHED_SCRATCH];
     const int q = blockIdx.x;
-    const int sub = threadIdx.x >> 7, t = threadIdx.x & 127;
-    const int h = blockIdx.y * 2 + sub;
     const int d_c = a.d_c;
+    const int quad0 = blockIdx.y * COMBINE_QUADS;
     const int np = query_pages(a.qs, q);
     const long long total = block_total_pages(a.qs, red);
     long long per = (total + a.n_units - 1) / a.n_units;
     if (per < 1) per = 1;
     const long long pq = block_prefix_pages(a.qs, q, red);
-    if (h >= a.n_h) return;
-    T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * a.n_h + h) * d_c;
-    if (np == 0) {
-        for (int c = t; c < d_c; c += 128) out[c] = from_f32<T>(0.f);
-        if (t == 0) a.lse[(long long)q * a.n_h + h] = -INFINITY;
-        return;
-    }
-    const long long u_lo = pq / per, u_hi = (pq + np - 1) / per;
-    if (u_lo == u_hi) return;  // written directly by the attention kernel
+    const long long u_lo = pq / per, u_hi = np > 0 ? (pq + np - 1) / per : u_lo;
+    if (np > 0 && u_lo == u_hi) return;  // written directly by the attention kernel
     auto slot_of = [&](long long u) { return (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1; };
-    float mx = -INFINITY;
-    for (long long u = u_lo; u <= u_hi; ++u) mx = fmaxf(mx, a.part_lse[slot_of(u) * a.n_h + h]);
-    float wsum = 0.f;
-    for (long long u = u_lo; u <= u_hi; ++u) {
-        const float l = a.part_lse[slot_of(u) * a.n_h + h];
-        wsum += (l == -INFINITY) ? 0.f : __expf(l - mx);
-    }
-    const float inv = 1.f / wsum;
-    for (int c = 4 * t; c < d_c; c += 512) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (long long u = u_lo; u <= u_hi; ++u) {
-            const long long sl = slot_of(u);
+    for (int h = threadIdx.x; h < a.n_h; h += blockDim.x) {
+        T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * a.n_h + h) * d_c;
+        if (np == 0) {
+            for (int c = quad0 * 4; c < min(d_c, (quad0 + COMBINE_QUADS) * 4); ++c) out[c] = from_f32<T>(0.f);
+            if (blockIdx.y == 0) a.lse[(long long)q * a.n_h + h] = -INFINITY;
+            continue;
+        }
+        // slot weights once (independent loads), then for each slot eight independent
+        // float4 loads: the chain length is the number of slots, not slots x quads
+        const int ns = (int)(u_hi - u_lo + 1);
+        float mx = -INFINITY;
+        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, a.part_lse[slot_of(u_lo + i) * a.n_h + h]);
+        float wsum = 0.f;
+        for (int i = 0; i < ns; ++i) {
+            const float l = a.part_lse[slot_of(u_lo + i) * a.n_h + h];
+            wsum += (l == -INFINITY) ? 0.f : __expf(l - mx);
+        }
+        const float inv = 1.f / wsum;
+        const int nq = min(COMBINE_QUADS, d_c / 4 - quad0);
+        float4 acc[COMBINE_QUADS];
+#pragma unroll
+        for (int j = 0; j < COMBINE_QUADS; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < ns; ++i) {
+            const long long sl = slot_of(u_lo + i);
             const float l = a.part_lse[sl * a.n_h + h];
             const float w = (l == -INFINITY) ? 0.f : __expf(l - mx) * inv;
-            const float4 v = *reinterpret_cast<const float4*>(a.part_o + (sl * a.n_h + h) * d_c + c);
-            acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+            const float4* src = reinterpret_cast<const float4*>(a.part_o + part_index(sl, h, 4 * quad0, a.n_h, d_c));
+            float4 v[COMBINE_QUADS];
+#pragma unroll
+            for (int j = 0; j < COMBINE_QUADS; ++j) v[j] = j < nq ? src[(size_t)j * a.n_h] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < COMBINE_QUADS; ++j) {
+                acc[j].x = fmaf(w, v[j].x, acc[j].x); acc[j].y = fmaf(w, v[j].y, acc[j].y);
+                acc[j].z = fmaf(w, v[j].z, acc[j].z); acc[j].w = fmaf(w, v[j].w, acc[j].w);
+            }
         }
-        out[c] = from_f32<T>(acc.x);
-        if (c + 1 < d_c) out[c + 1] = from_f32<T>(acc.y);
-        if (c + 2 < d_c) out[c + 2] = from_f32<T>(acc.z);
-        if (c + 3 < d_c) out[c + 3] = from_f32<T>(acc.w);
+#pragma unroll
+        for (int j = 0; j < COMBINE_QUADS; ++j) {
+            if (j < nq) {
+                const int c = 4 * (quad0 + j);
+                out[c] = from_f32<T>(acc[j].x);
+                out[c + 1] = from_f32<T>(acc[j].y);
+                out[c + 2] = from_f32<T>(acc[j].z);
+                out[c + 3] = from_f32<T>(acc[j].w);
+            }
+        }
+        if (blockIdx.y == 0) a.lse[(long long)q * a.n_h + h] = mx + logf(wsum);
     }
-    if (t == 0) a.lse[(long long)q * a.n_h + h] = mx + logf(wsum);
 }
 
 }  // namespace mla

@@ -127,23 +127,27 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs g) {
 }
 
 // RoPE part of the absorbed query: q_cat[n,h,d_c+2i : d_c+2i+2] = rotate(q_rope[n,h,2i:2i+2], pos[n]).
-// One block per token: the d_r/2 angles are evaluated once (double precision) into shared
-// memory and shared by all heads.
+// Grid (n_tokens, ceil(n_h / ROPE_HEADS)): the d_r/2 angles of the token are evaluated once per
+// block (double precision) into shared memory; each thread then rotates a few pairs.
+constexpr int ROPE_HEADS = 16;
+
 template <typename T>
 __global__ void __launch_bounds__(256) rope_query_kernel(const T* __restrict__ q_rope, const int* __restrict__ pos,
                                                          T* __restrict__ q_cat, int n_tokens, int n_h, int d_r,
                                                          int d_c, float base) {
     __shared__ float cs[512], sn[512];   // d_r <= 1024
     const int n = blockIdx.x;
+    const int h0 = blockIdx.y * ROPE_HEADS;
     const int half = d_r / 2;
     const int p = __ldg(pos + n);
     for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(p, i, d_r, base, &cs[i], &sn[i]);
     __syncthreads();
-    for (int e = threadIdx.x; e < n_h * half; e += blockDim.x) {
-        const int h = e / half, i = e % half;
-        const long long nh = (long long)n * n_h + h;
-        const T* src = q_rope + nh * d_r + 2 * i;
-        T* dst = q_cat + nh * (long long)(d_c + d_r) + d_c + 2 * i;
+    const int nh = min(ROPE_HEADS, n_h - h0);
+    for (int e = threadIdx.x; e < nh * half; e += blockDim.x) {
+        const int h = h0 + e / half, i = e % half;
+        const long long row = (long long)n * n_h + h;
+        const T* src = q_rope + row * d_r + 2 * i;
+        T* dst = q_cat + row * (long long)(d_c + d_r) + d_c + 2 * i;
         const float x0 = to_f32(src[0]), x1 = to_f32(src[1]);
         dst[0] = from_f32<T>(x0 * cs[i] - x1 * sn[i]);
         dst[1] = from_f32<T>(x0 * sn[i] + x1 * cs[i]);

@@ -18,10 +18,11 @@
 //     rescales O rows when alpha != 1, then O += P . page[:, 0:512] with P as the
 //     shared-memory A operand; drains O / l at the end of every segment.
 //
-// Each page is read from HBM once: its eight 64-column latent chunks are TMA-multicast to
-// both CTAs (each CTA issues four), the RoPE chunk goes to the score CTA only.  A stage is
-// refilled when both CTAs have released it (commits multicast to both empty barriers).  The
-// score-to-value traffic is one-directional, so neither CTA waits on a round trip.
+// Each CTA streams the page through its own 3-stage TMA ring (the score CTA all 576 columns,
+// the value CTA the 512 latent ones), so the score CTA recycles a stage right after its QK
+// instead of holding it until the value CTA's PV; the value CTA's copy of the latent columns
+// is read while the line is still in L2.  The score-to-value traffic is one-directional, so
+// neither CTA waits on a round trip.
 //
 // Roles (192 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
 // (one TMEM lane quarter each, one head per thread) softmax in the score CTA, rescale and
@@ -40,18 +41,19 @@ namespace tca {
 constexpr int NH = 128, DC = 512, DR = 64, WID = 576, PAGE = 64;
 constexpr int CHUNK = 64 * 128;                   // 64 rows x 64 bf16, 128-byte swizzled
 constexpr int LAT_CHUNKS = 8;
-constexpr int STAGE_BYTES = LAT_CHUNKS * CHUNK;   // 64 KB latent part of a page
 constexpr int STAGES = 3;
-constexpr int OFF_R = STAGES * STAGE_BYTES;       // score CTA: RoPE chunks; value CTA: P buffers
+constexpr int S_STAGE_BYTES = 9 * CHUNK;          // score CTA: whole page, 9 chunks (72 KB)
+constexpr int V_STAGE_BYTES = LAT_CHUNKS * CHUNK; // value CTA: latent part (64 KB)
+constexpr int OFF_R = STAGES * V_STAGE_BYTES;     // value CTA: P buffers
 constexpr int P_BYTES = NH * 128;                 // P [128 heads x 64 tokens] bf16, SW128 K-major
 constexpr int META_BYTES = NH * 8;                // (alpha, l) per head, fp32
 constexpr int PBUF_BYTES = P_BYTES + META_BYTES;
 constexpr int R_BYTES = 2 * PBUF_BYTES;
-static_assert(R_BYTES >= STAGES * CHUNK, "RoPE stages must fit the shared region");
-constexpr int OFF_BARS = OFF_R + R_BYTES;
+constexpr int OFF_BARS = OFF_R + R_BYTES;         // same offset in both CTAs
+static_assert(STAGES * S_STAGE_BYTES <= OFF_BARS, "score CTA stages must fit below the barriers");
 enum {
-    B_FULL = 0,                  // [STAGES] page landed (own expect_tx + bytes from both issuers)
-    B_EMPTY = B_FULL + STAGES,   // [STAGES] both CTAs released the stage (2 commits)
+    B_FULL = 0,                  // [STAGES] page landed in this CTA's ring
+    B_EMPTY = B_FULL + STAGES,   // [STAGES] this CTA's consumer released the stage
     B_SFULL = B_EMPTY + STAGES,  // [2] score CTA: S buffer written
     B_SFREE = B_SFULL + 2,       // [2] score CTA: S buffer read by the 4 softmax warps
     B_QFULL = B_SFREE + 2,       // score CTA: Q of the segment in TMEM
@@ -61,6 +63,7 @@ enum {
     B_PVDONE = B_PREADY + 2,     // [2] value CTA: PV of the page that used P buffer b complete
     B_OFREE = B_PVDONE + 2,      // value CTA: O drained
     B_DONE = B_OFREE + 1,        // MMA drain at exit
+    B_START = B_DONE + 1,        // score CTA: first page's TMA issued (Q loads go after it)
     NBARS
 };
 constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
@@ -130,15 +133,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + OFF_BARS + 8u * (uint32_t)i; }
 
 // ----------------------------------------------------------------------------- warp 0: TMA
-// Both CTAs run the same page sequence; rank 0 issues latent chunks 0-3 (multicast) and the
-// RoPE chunk (local), rank 1 issues latent chunks 4-7 (multicast).
+// Both CTAs run the same page sequence; the score CTA loads all nine 64-column chunks of a
+// page, the value CTA the eight latent chunks.
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tm, UnitCursor c, uint32_t base,
                                          uint32_t rank, const WaitCtl& wc) {
     uint32_t g = 0;
     bool ok = true;
     Segment sg;
-    const uint32_t expect = rank == 0 ? (uint32_t)(STAGE_BYTES + CHUNK) : (uint32_t)STAGE_BYTES;
-    const int c0 = rank == 0 ? 0 : 4;
+    const int nch = rank == 0 ? 9 : LAT_CHUNKS;
+    const uint32_t stage_bytes = (uint32_t)(nch * CHUNK);
     while (ok && c.next(a.qs, &sg)) {
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const uint32_t stage = g % STAGES;
@@ -149,11 +152,10 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                 page = 0;  // keep the pipeline fed; the result of this query is void
             }
             const uint32_t fb = bar_addr(base, B_FULL + stage);
-            ptx::mbar_arrive_expect_tx(fb, expect);
-            const uint32_t dst = base + stage * STAGE_BYTES;
-            for (int cc = c0; cc < c0 + 4; ++cc)
-                ptx::tma_load_2d_mc(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb, (uint16_t)0x3);
-            if (rank == 0) ptx::tma_load_2d(base + OFF_R + stage * CHUNK, tm, DC, page * PAGE, fb);
+            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+            const uint32_t dst = base + stage * stage_bytes;
+            for (int cc = 0; cc < nch; ++cc) ptx::tma_load_2d(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
+            if (g == 0) ptx::mbar_arrive(bar_addr(base, B_START));
         }
     }
     if (!ok) {  // let loads already in flight land before the CTA leaves
@@ -178,17 +180,19 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
             if (pg == sg.page_begin && !wait_bar(bar_addr(base, B_QFULL), segn & 1u, wc)) { ok = false; break; }
             if (!wait_bar(bar_addr(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t st = base + stage * STAGE_BYTES;
+            // fully unrolled issue: descriptors are the stage's base descriptor plus constant
+            // offsets (the 14-bit address field cannot carry: shared addresses are < 256 KB)
+            const uint64_t d_pg = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
             const uint32_t d = tmem + TM_S + sb * 64;
+#pragma unroll
             for (int cc = 0; cc < 9; ++cc) {
-                const uint32_t cb = cc < LAT_CHUNKS ? st + cc * CHUNK : base + OFF_R + stage * CHUNK;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA, 4 per 64-column chunk
-                    ptx::mma_ts(d, tmem + TM_Q + cc * 32 + kk * 8, ptx::desc_sw128(cb + kk * 32, 16, 1024), IDESC_QK,
-                                (cc | kk) ? 1u : 0u);
+                    ptx::mma_ts(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
+                                IDESC_QK, (cc | kk) ? 1u : 0u);
             }
             ptx::tc_commit(bar_addr(base, B_SFULL + sb));
-            ptx::tc_commit_mc(bar_addr(base, B_EMPTY + stage), (uint16_t)0x3);
+            ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
         }
         ++segn;
     }
@@ -212,18 +216,30 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
     uint32_t g = 0;
     bool ok = true;
     Segment sg;
+    bool started = false;
     while (ok && c.next(a.qs, &sg)) {
-        // this segment's query row into TMEM; the previous segment's QK MMAs are complete
-        // because their S was consumed
+        // the first page's TMA goes out before this CTA's query loads fill the load queues
+        if (!started) {
+            if (!warp_wait(bar_addr(base, B_START), 0, wc, false, lane)) { ok = false; break; }
+            started = true;
+        }
+        // this segment's query row into TMEM (three chunks per batch of loads in flight); the
+        // previous segment's QK MMAs are complete because their S was consumed
         const uint4* qrow = reinterpret_cast<const uint4*>(qc + ((size_t)sg.q * NH + h) * WID);
-        for (int cc = 0; cc < 9; ++cc) {
-            uint32_t r[32];
+        for (int c3 = 0; c3 < 9; c3 += 3) {
+            uint4 v[24];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 v = __ldg(qrow + cc * 8 + i);
-                r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+            for (int i = 0; i < 24; ++i) v[i] = __ldg(qrow + c3 * 8 + i);
+#pragma unroll
+            for (int cc = 0; cc < 3; ++cc) {
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    r[4 * i] = v[cc * 8 + i].x; r[4 * i + 1] = v[cc * 8 + i].y;
+                    r[4 * i + 2] = v[cc * 8 + i].z; r[4 * i + 3] = v[cc * 8 + i].w;
+                }
+                ptx::tmem_st32(tQ + (c3 + cc) * 32, r);
             }
-            ptx::tmem_st32(tQ + cc * 32, r);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -306,18 +322,18 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
             if (!wait_bar(bar_addr(base, B_PREADY + pb), (g >> 1) & 1u, wc)) { ok = false; break; }
             if (first && segn > 0 && !wait_bar(bar_addr(base, B_OFREE), (segn - 1) & 1u, wc)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t st = base + stage * STAGE_BYTES;
-            const uint32_t pa = base + OFF_R + pb * PBUF_BYTES;
+            const uint64_t da = ptx::desc_sw128(base + OFF_R + pb * PBUF_BYTES, 16, 1024);
+            const uint64_t db = ptx::desc_sw128(base + stage * V_STAGE_BYTES, CHUNK, 1024);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // 16 tokens per MMA; V is MN-major: chunks 8 KB apart
-                    ptx::mma_ss(tmem + TM_O + hf * 256, ptx::desc_sw128(pa + kk * 32, 16, 1024),
-                                ptx::desc_sw128(st + hf * 4 * CHUNK + kk * 2048, CHUNK, 1024), IDESC_PV,
+                    ptx::mma_ss(tmem + TM_O + hf * 256, da + (uint64_t)((kk * 32) >> 4),
+                                db + (uint64_t)((hf * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV,
                                 (first && kk == 0) ? 0u : 1u);
             }
             ptx::tc_commit(bar_addr(base, B_PVDONE + pb));
-            ptx::tc_commit_mc(bar_addr(base, B_EMPTY + stage), (uint16_t)0x3);
+            ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
             ptx::tc_commit_mc(bar_addr(base, B_PEMPTY + pb), (uint16_t)0x1);
         }
         ++segn;
@@ -396,11 +412,12 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
                     d4[i] = v;
                 }
             } else {
-                float4* d4 = reinterpret_cast<float4*>(a.part_o + ((size_t)sg.slot * NH + h) * DC + 32 * k);
+                // partial layout [slot][c/4][h][c%4]: a warp's 32 heads write 512 contiguous bytes
+                float4* d4 = reinterpret_cast<float4*>(a.part_o) + ((size_t)sg.slot * (DC / 4) + 8 * k) * NH + h;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                        __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+                    d4[(size_t)i * NH] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                                     __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
             }
         }
         ptx::tc_fence_before();
@@ -430,7 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_addr(base, B_FULL + s), 1);
-            ptx::mbar_init(bar_addr(base, B_EMPTY + s), 2);
+            ptx::mbar_init(bar_addr(base, B_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr(base, B_SFULL + b), 1);
@@ -443,6 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         ptx::mbar_init(bar_addr(base, B_QFULL), 4);
         ptx::mbar_init(bar_addr(base, B_OFREE), 4);
         ptx::mbar_init(bar_addr(base, B_DONE), 1);
+        ptx::mbar_init(bar_addr(base, B_START), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -540,14 +558,6 @@ inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache,
 inline bool tc_gemm_append_supported(const mla_config*, int) { return false; }
 inline mla_status tc_gemm_append(const mla_config*, const mla_cache*, const void*, const void*, const void*,
                                  const int32_t*, const int32_t*, int32_t, cudaStream_t) {
-    return MLA_ERR_UNSUPPORTED;
-}
-inline bool tc_gemm_absorb_supported(const mla_config*, int) { return false; }
-inline mla_status tc_gemm_absorb(const mla_config*, const void*, const void*, void*, int32_t, cudaStream_t) {
-    return MLA_ERR_UNSUPPORTED;
-}
-inline bool tc_gemm_out_supported(const mla_config*, int) { return false; }
-inline mla_status tc_gemm_out(const mla_config*, const void*, const void*, void*, int32_t, cudaStream_t) {
     return MLA_ERR_UNSUPPORTED;
 }
 

@@ -1,0 +1,258 @@
+// tcgen05 GEMM for the per-head projections around the attention (sm_103a, bf16, fp32 acc).
+//
+//   absorb: q_cat[n, h, c] = sum_j W_UK[c, h*d_h + j] * q_nope[n, h, j]      (M = c, K = j)
+//   out:    o[n, h*d_h + j] = sum_c W_UV[c, h*d_h + j] * o_lat[n, h, c]       (M = j, K = c)
+//
+// Both are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
+// 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, as the weight is stored) and
+// up to 256 tokens as B (K-major).  With few tokens (decode) the tile streams the weights
+// once at HBM speed; with many (prefill) the grid tiles the tokens.  Each CTA owns one
+// (m-tile, head, n-tile): warp 0 TMA-loads 64-wide K chunks of A and B into a 4-stage ring,
+// warp 1 issues the MMAs into TMEM, warps 2-5 drain D (one row per thread).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace tcg {
+
+constexpr int BM = 128, BK = 64, MAX_N = 256, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int NTHREADS = 192;
+
+// stage = A tile + B tile (n_pad rows of 128 B), rounded to the 1 KB swizzle atom
+__host__ __device__ inline int stage_bytes(int n_pad) { return (A_BYTES + n_pad * BK * 2 + 1023) & ~1023; }
+__host__ __device__ inline int smem_bytes(int n_pad) { return STAGES * stage_bytes(n_pad) + 128; }
+__host__ __device__ inline uint32_t tmem_cols(int n_pad) {
+    uint32_t c = 32;
+    while ((int)c < n_pad) c <<= 1;
+    return c;
+}
+
+enum Mode { ABSORB = 0, OUT = 1 };
+
+struct GemmArgs {
+    int mode;
+    int n_tokens;       // valid tokens
+    int n_pad;          // MMA N (multiple of 16, >= 16, <= 256)
+    int k_chunks;       // K / 64
+    int n_h, d_h, d_c, width;
+    void* out;          // q_cat (ABSORB) or o (OUT), bf16
+    unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned long long limit) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            const unsigned long long t = globaltimer_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > limit) {
+                set_device_error(MLA_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// grid: (m-tiles, n_h, n-tiles)
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t base = ptx::smem_u32(smem);
+    if (base & 1023u) {
+        if (threadIdx.x == 0) set_device_error(MLA_ERR_UNSUPPORTED);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * MAX_N;
+    const int SB = stage_bytes(g.n_pad);
+    const uint32_t ncols = tmem_cols(g.n_pad);
+    const uint32_t bar_full = base + STAGES * SB, bar_empty = bar_full + 8 * STAGES, bar_done = bar_empty + 8 * STAGES;
+    const uint32_t slot = bar_done + 8;
+    const bool a_mn = g.mode == OUT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        ptx::mbar_init(bar_done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(slot, ncols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem + (slot - base));
+    bool ok = true;
+
+    if (warp == 0 && lane == 0) {
+        const uint32_t bytes = (uint32_t)(A_BYTES + g.n_pad * BK * 2);
+        for (int kc = 0; kc < g.k_chunks; ++kc) {
+            const int s = kc % STAGES;
+            if (!gwait(bar_empty + 8 * s, ((kc / STAGES) & 1u) ^ 1u, g.wait_ns)) { ok = false; break; }
+            const uint32_t st = base + s * SB, fb = bar_full + 8 * s;
+            ptx::mbar_arrive_expect_tx(fb, bytes);
+            if (g.mode == ABSORB) {
+                // A: W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
+                ptx::tma_load_2d(st, &tmA, h * g.d_h + kc * BK, mt * BM, fb);
+                // B: q_nope viewed [n, n_h*d_h]: cols h*d_h + kc*64, rows n0 .. n0 + n_pad
+                ptx::tma_load_2d(st + A_BYTES, &tmB, h * g.d_h + kc * BK, n0, fb);
+            } else {
+                // A: W_UV rows c in [kc*64, +64) x cols h*d_h + mt*128 + {0, 64} (MN-major, two boxes)
+                ptx::tma_load_2d(st, &tmA, h * g.d_h + mt * BM, kc * BK, fb);
+                ptx::tma_load_2d(st + BK * 128, &tmA, h * g.d_h + mt * BM + 64, kc * BK, fb);
+                // B: o_lat viewed [n, n_h*d_c]: cols h*d_c + kc*64
+                ptx::tma_load_2d(st + A_BYTES, &tmB, h * g.d_c + kc * BK, n0, fb);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        const uint32_t idesc = ptx::idesc_bf16(BM, g.n_pad, a_mn, false);
+        for (int kc = 0; kc < g.k_chunks; ++kc) {
+            const int s = kc % STAGES;
+            if (!gwait(bar_full + 8 * s, (kc / STAGES) & 1u, g.wait_ns)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t st = base + s * SB;
+            const uint64_t da = a_mn ? ptx::desc_sw128(st, BK * 128, 1024) : ptx::desc_sw128(st, 16, 1024);
+            const uint64_t db = ptx::desc_sw128(st + A_BYTES, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                // K-major A: +32 B per 16-wide K step; MN-major A: +16 rows of 128 B
+                const uint64_t a_off = a_mn ? (uint64_t)((kk * 2048) >> 4) : (uint64_t)((kk * 32) >> 4);
+                ptx::mma_ss(tmem, da + a_off, db + (uint64_t)((kk * 32) >> 4), idesc, (kc | kk) ? 1u : 0u);
+            }
+            ptx::tc_commit(bar_empty + 8 * s);
+        }
+        ptx::tc_commit(bar_done);
+    } else if (warp >= 2) {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;  // m within the tile
+        if (gwait(bar_done, 0, g.wait_ns)) {
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
+            bf16* out = reinterpret_cast<bf16*>(g.out);
+            for (int c0 = 0; c0 < g.n_pad; c0 += 32) {  // reads stay inside the allocation (>= 32 columns)
+                uint32_t r[32];
+                ptx::tmem_ld32(taddr + c0, r);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = n0 + c0 + j;
+                    if (c0 + j < g.n_pad && n < g.n_tokens) {
+                        const bf16 v = __float2bfloat16_rn(__uint_as_float(r[j]));
+                        if (g.mode == ABSORB)
+                            out[((size_t)n * g.n_h + h) * g.width + mt * BM + row] = v;
+                        else
+                            out[(size_t)n * g.n_h * g.d_h + (size_t)h * g.d_h + mt * BM + row] = v;
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, ncols);
+    }
+}
+
+// 2-D bf16 map: inner extent `inner` elements with row pitch `pitch_elems`, `rows` rows, box
+// (64, box_rows), 128-byte swizzle; reads past the extents return zeros.
+inline bool encode_2d(CUtensorMap* tm, const void* p, uint64_t inner, uint64_t rows, uint64_t pitch_elems,
+                      uint32_t box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) !=
+                cudaSuccess ||
+            r != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(q);
+    }
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {pitch_elems * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int n_pad_for(int n) {
+    int p = n < MAX_N ? n : MAX_N;
+    return (p + 15) & ~15;
+}
+
+inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtensorMap& b, int m_tiles, int n_h,
+                         cudaStream_t stream) {
+    GemmArgs g = g0;
+    const int smem = smem_bytes(g.n_pad);
+    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    dim3 grid(m_tiles, n_h, (g.n_tokens + MAX_N - 1) / MAX_N);
+    tc_gemm_kernel<<<grid, NTHREADS, smem, stream>>>(a, b, g);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace tcg
+
+inline bool tc_gemm_absorb_supported(const mla_config* c, int n, int cc_major, int cc_minor) {
+    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 && c->d_nope % 64 == 0 &&
+           c->d_latent % 128 == 0 && ((long long)c->n_heads * c->d_nope) % 8 == 0;
+}
+inline bool tc_gemm_out_supported(const mla_config* c, int n, int cc_major, int cc_minor) {
+    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 && c->d_nope % 128 == 0 &&
+           c->d_latent % 64 == 0;
+}
+
+// q_cat[:, :, 0:d_c] of mla_absorb_q (the RoPE half is written by rope_query_kernel)
+inline mla_status tc_gemm_absorb(const mla_config* c, const void* q_nope, const void* w_uk, void* q_cat, int n,
+                                 unsigned long long wait_ns, cudaStream_t stream) {
+    tcg::GemmArgs g{};
+    g.mode = tcg::ABSORB;
+    g.n_tokens = n;
+    g.n_pad = tcg::n_pad_for(n);
+    g.k_chunks = c->d_nope / tcg::BK;
+    g.n_h = c->n_heads; g.d_h = c->d_nope; g.d_c = c->d_latent; g.width = c->d_latent + c->d_rope;
+    g.out = q_cat;
+    g.wait_ns = wait_ns;
+    const uint64_t hd = (uint64_t)c->n_heads * c->d_nope;
+    CUtensorMap ta, tb;
+    if (!tcg::encode_2d(&ta, w_uk, hd, (uint64_t)c->d_latent, hd, tcg::BM) ||
+        !tcg::encode_2d(&tb, q_nope, hd, (uint64_t)n, hd, (uint32_t)g.n_pad))
+        return MLA_ERR_CUDA;
+    return tcg::launch(g, ta, tb, c->d_latent / tcg::BM, c->n_heads, stream);
+}
+
+inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void* w_uv, void* o, int n,
+                              unsigned long long wait_ns, cudaStream_t stream) {
+    tcg::GemmArgs g{};
+    g.mode = tcg::OUT;
+    g.n_tokens = n;
+    g.n_pad = tcg::n_pad_for(n);
+    g.k_chunks = c->d_latent / tcg::BK;
+    g.n_h = c->n_heads; g.d_h = c->d_nope; g.d_c = c->d_latent; g.width = c->d_latent + c->d_rope;
+    g.out = o;
+    g.wait_ns = wait_ns;
+    const uint64_t hd = (uint64_t)c->n_heads * c->d_nope, hc = (uint64_t)c->n_heads * c->d_latent;
+    CUtensorMap ta, tb;
+    if (!tcg::encode_2d(&ta, w_uv, hd, (uint64_t)c->d_latent, hd, 64) ||
+        !tcg::encode_2d(&tb, o_lat, hc, (uint64_t)n, hc, (uint32_t)g.n_pad))
+        return MLA_ERR_CUDA;
+    return tcg::launch(g, ta, tb, c->d_nope / tcg::BM, c->n_heads, stream);
+}
+
+}  // namespace mla
