@@ -24,6 +24,10 @@
 // is read while the line is still in L2.  The score-to-value traffic is one-directional, so
 // neither CTA waits on a round trip.
 //
+// The query of a segment travels through the score CTA's ring too: three items of three
+// 128-row x 64-column chunks, TMA-loaded and copied into TMEM by the MMA thread with
+// tcgen05.cp ahead of the segment's first QK (the tensor pipe keeps issue order).
+//
 // Roles (192 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
 // (one TMEM lane quarter each, one head per thread) softmax in the score CTA, rescale and
 // drain in the value CTA.  Every wait is bounded.
@@ -43,6 +47,8 @@ constexpr int CHUNK = 64 * 128;                   // 64 rows x 64 bf16, 128-byte
 constexpr int LAT_CHUNKS = 8;
 constexpr int STAGES = 3;
 constexpr int S_STAGE_BYTES = 9 * CHUNK;          // score CTA: whole page, 9 chunks (72 KB)
+constexpr int Q_CHUNK = 128 * 128;                // 128 query rows x 64 bf16 (16 KB)
+constexpr int Q_ITEMS = 3;                        // ring items per query, three chunks each
 constexpr int V_STAGE_BYTES = LAT_CHUNKS * CHUNK; // value CTA: latent part (64 KB)
 constexpr int OFF_R = STAGES * V_STAGE_BYTES;     // value CTA: P buffers
 constexpr int P_BYTES = NH * 128;                 // P [128 heads x 64 tokens] bf16, SW128 K-major
@@ -56,14 +62,12 @@ enum {
     B_EMPTY = B_FULL + STAGES,   // [STAGES] this CTA's consumer released the stage
     B_SFULL = B_EMPTY + STAGES,  // [2] score CTA: S buffer written
     B_SFREE = B_SFULL + 2,       // [2] score CTA: S buffer read by the 4 softmax warps
-    B_QFULL = B_SFREE + 2,       // score CTA: Q of the segment in TMEM
-    B_PFULL = B_QFULL + 1,       // [2] value CTA: P + meta landed (own expect_tx + bytes)
+    B_PFULL = B_SFREE + 2,       // [2] value CTA: P + meta landed (own expect_tx + bytes)
     B_PEMPTY = B_PFULL + 2,      // [2] score CTA: value CTA's PV finished with P buffer b
     B_PREADY = B_PEMPTY + 2,     // [2] value CTA: O rescaled, P buffer b ready for the MMA
     B_PVDONE = B_PREADY + 2,     // [2] value CTA: PV of the page that used P buffer b complete
     B_OFREE = B_PVDONE + 2,      // value CTA: O drained
     B_DONE = B_OFREE + 1,        // MMA drain at exit
-    B_START = B_DONE + 1,        // score CTA: first page's TMA issued (Q loads go after it)
     NBARS
 };
 constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
@@ -135,14 +139,24 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 // ----------------------------------------------------------------------------- warp 0: TMA
 // Both CTAs run the same page sequence; the score CTA loads all nine 64-column chunks of a
 // page, the value CTA the eight latent chunks.
-__device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tm, UnitCursor c, uint32_t base,
-                                         uint32_t rank, const WaitCtl& wc) {
-    uint32_t g = 0;
+__device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tm, const CUtensorMap* tmq, UnitCursor c,
+                                         uint32_t base, uint32_t rank, const WaitCtl& wc) {
+    uint32_t g = 0;  // ring items issued
     bool ok = true;
     Segment sg;
     const int nch = rank == 0 ? 9 : LAT_CHUNKS;
     const uint32_t stage_bytes = (uint32_t)(nch * CHUNK);
     while (ok && c.next(a.qs, &sg)) {
+        if (rank == 0) {  // the segment's query: three ring items of three 16 KB chunks
+            for (int qi = 0; qi < Q_ITEMS; ++qi, ++g) {
+                const uint32_t stage = g % STAGES;
+                if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
+                const uint32_t fb = bar_addr(base, B_FULL + stage), dst = base + stage * S_STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)(3 * Q_CHUNK));
+                for (int j = 0; j < 3; ++j) ptx::tma_load_2d(dst + j * Q_CHUNK, tmq, (3 * qi + j) * 64, sg.q * NH, fb);
+            }
+            if (!ok) break;
+        }
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const uint32_t stage = g % STAGES;
             if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
@@ -155,7 +169,6 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             ptx::mbar_arrive_expect_tx(fb, stage_bytes);
             const uint32_t dst = base + stage * stage_bytes;
             for (int cc = 0; cc < nch; ++cc) ptx::tma_load_2d(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
-            if (g == 0) ptx::mbar_arrive(bar_addr(base, B_START));
         }
     }
     if (!ok) {  // let loads already in flight land before the CTA leaves
@@ -170,14 +183,31 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
 // ----------------------------------------------------------------------------- score CTA
 __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
                                           const WaitCtl& wc) {
-    uint32_t g = 0, segn = 0;
+    uint32_t g = 0, k = 0;  // pages, ring items
     bool ok = true;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
-        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
-            const uint32_t stage = g % STAGES, sb = g & 1u;
-            if (!wait_bar(bar_addr(base, B_FULL + stage), (g / STAGES) & 1u, wc)) { ok = false; break; }
-            if (pg == sg.page_begin && !wait_bar(bar_addr(base, B_QFULL), segn & 1u, wc)) { ok = false; break; }
+        // the segment's query into TMEM columns [TM_Q, TM_Q + 288).  A copy is ordered before
+        // the MMAs issued after it, but not after those issued before it: the previous
+        // segment's last QK (whose commit covers all earlier ones) must finish reading Q first.
+        if (g > 0 && !wait_bar(bar_addr(base, B_SFULL + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u, wc)) break;
+        for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) {
+            const uint32_t stage = k % STAGES;
+            if (!wait_bar(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint64_t dq = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    ptx::tmem_cp_128x256b(tmem + TM_Q + (3 * qi + j) * 32 + kk * 8,
+                                          dq + (uint64_t)((j * Q_CHUNK + kk * 32) >> 4));
+            ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
+        }
+        if (!ok) break;
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
+            const uint32_t stage = k % STAGES, sb = g & 1u;
+            if (!wait_bar(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
             if (!wait_bar(bar_addr(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
             ptx::tc_fence_after();
             // fully unrolled issue: descriptors are the stage's base descriptor plus constant
@@ -194,7 +224,6 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
             ptx::tc_commit(bar_addr(base, B_SFULL + sb));
             ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
         }
-        ++segn;
     }
     ptx::tc_commit(bar_addr(base, B_DONE));
     WaitCtl w2 = wc;
@@ -208,44 +237,14 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
     const int qd = warp & 3;  // TMEM lane quarter this warp may access
     const int h = qd * 32 + lane;
     const uint32_t lb = (uint32_t)(qd * 32) << 16;
-    const uint32_t tQ = tmem + lb + TM_Q, tS = tmem + lb + TM_S;
+    const uint32_t tS = tmem + lb + TM_S;
     const uint32_t pbuf_r = ptx::mapa(base + OFF_R, peer);          // value CTA's P buffers
     const uint32_t pfull_r = ptx::mapa(bar_addr(base, B_PFULL), peer);
     const uint32_t sw = (uint32_t)(h & 7);
-    const bf16* qc = reinterpret_cast<const bf16*>(a.q_cat);
     uint32_t g = 0;
     bool ok = true;
     Segment sg;
-    bool started = false;
     while (ok && c.next(a.qs, &sg)) {
-        // the first page's TMA goes out before this CTA's query loads fill the load queues
-        if (!started) {
-            if (!warp_wait(bar_addr(base, B_START), 0, wc, false, lane)) { ok = false; break; }
-            started = true;
-        }
-        // this segment's query row into TMEM (three chunks per batch of loads in flight); the
-        // previous segment's QK MMAs are complete because their S was consumed
-        const uint4* qrow = reinterpret_cast<const uint4*>(qc + ((size_t)sg.q * NH + h) * WID);
-        for (int c3 = 0; c3 < 9; c3 += 3) {
-            uint4 v[24];
-#pragma unroll
-            for (int i = 0; i < 24; ++i) v[i] = __ldg(qrow + c3 * 8 + i);
-#pragma unroll
-            for (int cc = 0; cc < 3; ++cc) {
-                uint32_t r[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    r[4 * i] = v[cc * 8 + i].x; r[4 * i + 1] = v[cc * 8 + i].y;
-                    r[4 * i + 2] = v[cc * 8 + i].z; r[4 * i + 3] = v[cc * 8 + i].w;
-                }
-                ptx::tmem_st32(tQ + (c3 + cc) * 32, r);
-            }
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_QFULL));
-
         float m_run = -INFINITY, l = 0.f;
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const uint32_t sb = g & 1u, use = g >> 1;
@@ -427,7 +426,8 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    tc_attention_kernel(const __grid_constant__ CUtensorMap tmap, const TcArgs args) {
+    tc_attention_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmq,
+                        const TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const AttnArgs& a = args.a;
     const uint32_t base = ptx::smem_u32(smem);
@@ -457,14 +457,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             ptx::mbar_init(bar_addr(base, B_PREADY + b), 4);
             ptx::mbar_init(bar_addr(base, B_PVDONE + b), 1);
         }
-        ptx::mbar_init(bar_addr(base, B_QFULL), 4);
         ptx::mbar_init(bar_addr(base, B_OFREE), 4);
         ptx::mbar_init(bar_addr(base, B_DONE), 1);
-        ptx::mbar_init(bar_addr(base, B_START), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) ptx::prefetch_tmap(&tmap);
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmap);
+        ptx::prefetch_tmap(&tmq);
+    }
     if (warp == 1) {
         ptx::tmem_alloc(base + OFF_MISC, 512);
         ptx::tmem_relinquish();
@@ -481,7 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const WaitCtl wc{args.wait_ns, abort_flag, false};
 
     if (warp == 0) {
-        if (lane == 0) producer(a, &tmap, cur, base, rank, wc);
+        if (lane == 0) producer(a, &tmap, &tmq, cur, base, rank, wc);
     } else if (warp == 1) {
         if (lane == 0) {
             if (rank == 0) score_mma(a, cur, base, tmem, wc);
@@ -520,13 +521,14 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over the pool viewed as [num_pages*64 rows, 576 columns] bf16; box 64 x 64, 128B swizzle.
-inline bool encode_pool_map(CUtensorMap* tm, void* pool, long long num_pages) {
+// 2-D map over rows of 576 bf16 ([num_pages*64 rows, 576 columns]); box 64 columns x box_rows,
+// 128-byte swizzle.
+inline bool encode_pool_map(CUtensorMap* tm, void* pool, long long num_pages, uint32_t box_rows = 64) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)WID, (cuuint64_t)num_pages * PAGE};
     cuuint64_t strides[1] = {(cuuint64_t)WID * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -542,8 +544,11 @@ inline bool tc_attention_supported(const mla_config* c, const mla_cache* k, int 
 
 inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache, unsigned long long wait_ns,
                                       cudaStream_t stream) {
-    CUtensorMap tm;
+    CUtensorMap tm, tmq;
     if (!tca::encode_pool_map(&tm, cache->pool, cache->num_pages)) return MLA_ERR_CUDA;
+    // the query rows viewed as [n_queries * 128, 576] bf16, box 64 columns x 128 rows
+    if (!tca::encode_pool_map(&tmq, const_cast<void*>(a.q_cat), (long long)a.qs.n_queries * tca::NH / tca::PAGE, 128))
+        return MLA_ERR_CUDA;
     tca::TcArgs t;
     t.a = a;
     t.wait_ns = wait_ns;
@@ -551,7 +556,7 @@ inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache,
     if (cudaFuncSetAttribute(tca::tc_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tca::SMEM_BYTES) != cudaSuccess)
         return MLA_ERR_CUDA;
-    tca::tc_attention_kernel<<<2 * a.n_units, tca::NTHREADS, tca::SMEM_BYTES, stream>>>(tm, t);
+    tca::tc_attention_kernel<<<2 * a.n_units, tca::NTHREADS, tca::SMEM_BYTES, stream>>>(tm, tmq, t);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
