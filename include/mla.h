@@ -61,7 +61,9 @@ typedef enum {
     MLA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed                     */
     MLA_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query returned */
     MLA_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait ran out (device error word)   */
-    MLA_ERR_DEVICE_BOUNDS = 6   /* a page id / position outside the cache (device error word) */
+    MLA_ERR_DEVICE_BOUNDS = 6,  /* a page id / position outside the cache (device error word) */
+    MLA_ERR_SCRATCH_LIMIT = 7   /* mla_decode_static: the split scratch this configuration needs
+                                   on this device exceeds MLA_STATIC_SCRATCH_BYTES             */
 } mla_status;
 
 typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
@@ -140,6 +142,28 @@ MLA_API mla_status mla_workspace_size(const mla_config* cfg, size_t* bytes);
 MLA_API mla_status mla_decode(const mla_config* cfg, const mla_cache* cache, const void* q_cat,
                       void* o_lat, float* lse, void* workspace, size_t workspace_bytes,
                       mla_stream_t stream);
+
+/* mla_decode_static - mla_decode that allocates nothing and takes no workspace.  The pages
+ * have no counterpart: this is a calling convention, not a step of the method.  It serves
+ * callers that cannot hand in device memory per call, e.g. a plain C host program with no
+ * device allocator of its own, or a serving loop that must not call cudaMalloc / cudaFree
+ * (which may synchronise the device) between steps.
+ * The split partials go to one fixed array of MLA_STATIC_SCRATCH_BYTES (80 MiB) per device,
+ * part of the library's device image: enough for 128 heads x 512 latent columns on up to
+ * 159 SMs.  A configuration that needs more (mla_workspace_size() > the limit) is rejected
+ * with MLA_ERR_SCRATCH_LIMIT before anything is launched.
+ * The first call on each device is its set-up: it looks up that array's address (with the
+ * device current), and the driver may place the array in device memory at that moment (lazy
+ * module loading).  Make that first call before any stream capture begins; the calls after
+ * it allocate nothing.  Nothing in the array has to start
+ * at zero: every partial the combine reads is written earlier in the same call.
+ * Calls that overlap in time (other streams, other host threads, or an overlapping
+ * mla_decode_static on the same device) race on the one array: order them, e.g. on one stream.
+ * Arguments, outputs and the other errors are those of mla_decode. */
+#define MLA_STATIC_SCRATCH_BYTES ((size_t)80 << 20)
+MLA_API mla_status mla_decode_static(const mla_config* cfg, const mla_cache* cache,
+                                     const void* q_cat, void* o_lat, float* lse,
+                                     mla_stream_t stream);
 
 /* mla_prefill - causal attention of n_queries consecutive tokens of sequence `seq` against
  * that sequence's cache ([OPN] s.2 prefill chain with the causal mask of autoregressive

@@ -17,7 +17,7 @@ from . import _lib
 from ._lib import MLAError, MLA_F32, MLA_BF16  # noqa: F401
 
 __all__ = ["MLAConfig", "PagedCache", "mla_cache_append", "mla_absorb_q", "mla_workspace_size",
-           "mla_decode", "mla_prefill", "mla_out", "mla_get_device_error", "mla_set_tuning",
+           "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_get_device_error", "mla_set_tuning",
            "mla_last_attention_path", "MLAError", "lib"]
 
 
@@ -126,6 +126,16 @@ def mla_decode(cfg: MLAConfig, cache: PagedCache, q_cat, o_lat=None, lse=None, w
     st = lib().mla_decode(ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q_cat), _ptr(o_lat),
                           _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
     _lib.check(st, "mla_decode")
+    return o_lat, lse
+
+
+def mla_decode_static(cfg: MLAConfig, cache: PagedCache, q_cat, o_lat, lse, stream=None):
+    """mla_decode without a workspace: the library keeps the split partials in a fixed device
+    array of MLA_STATIC_SCRATCH_BYTES, so nothing is allocated here or in the call; the
+    outputs are the caller's.  Calls that overlap in time race on that array."""
+    st = lib().mla_decode_static(ctypes.byref(cfg.c()), ctypes.byref(cache.c()), _ptr(q_cat),
+                                 _ptr(o_lat), _ptr(lse), _stream(stream))
+    _lib.check(st, "mla_decode_static")
     return o_lat, lse
 
 

@@ -9,7 +9,10 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
 
 MLA_OK = 0
 STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
-                4: "MLA_ERR_WORKSPACE", 5: "MLA_ERR_DEVICE_TIMEOUT", 6: "MLA_ERR_DEVICE_BOUNDS"}
+                4: "MLA_ERR_WORKSPACE", 5: "MLA_ERR_DEVICE_TIMEOUT", 6: "MLA_ERR_DEVICE_BOUNDS",
+                7: "MLA_ERR_SCRATCH_LIMIT"}
+MLA_ERR_SCRATCH_LIMIT = 7
+MLA_STATIC_SCRATCH_BYTES = 80 << 20
 MLA_F32, MLA_BF16 = 0, 1
 MLA_TUNE_ATTN_UNITS, MLA_TUNE_FORCE_SIMT, MLA_TUNE_WAIT_LIMIT_US = 0, 1, 2
 
@@ -40,6 +43,7 @@ SIGNATURES = {
     "mla_absorb_q": (_I, [_CFG, _P, _P, _P, _P, _P, _I, _P]),
     "mla_workspace_size": (_I, [_CFG, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_decode": (_I, [_CFG, _CACHE, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_decode_static": (_I, [_CFG, _CACHE, _P, _P, _P, _P]),
     "mla_prefill": (_I, [_CFG, _CACHE, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_out": (_I, [_CFG, _P, _P, _P, _I, _P]),
     "mla_get_device_error": (_I, [_P]),

@@ -182,6 +182,7 @@ const char* mla_status_string(mla_status s) {
         case MLA_ERR_WORKSPACE: return "workspace missing or too small";
         case MLA_ERR_DEVICE_TIMEOUT: return "device bounded wait timed out";
         case MLA_ERR_DEVICE_BOUNDS: return "page id or position outside the cache";
+        case MLA_ERR_SCRATCH_LIMIT: return "configuration needs more split scratch than the fixed no-allocation array holds";
     }
     return "unknown status";
 }
@@ -300,6 +301,53 @@ mla_status mla_decode(const mla_config* cfg, const mla_cache* cache, const void*
     qs.max_len = cache->max_pages * cfg->page_size;
     return attention(cfg, cache, qs, q_cat, o_lat, lse, workspace, workspace_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------------------------- no-allocation decode
+// mla_decode_static is for callers that cannot allocate per call or hand in a buffer: a plain C
+// host program without a device allocator, or a serving loop in which cudaMalloc / cudaFree
+// (which may synchronise the device) are not allowed between steps.  Its split partials live
+// in this file-scope array, one per device, created with the module: the call allocates
+// nothing.  Nothing in it has to start at zero (each partial the combine reads is written
+// earlier in the same call); calls that overlap in time race on it.
+namespace mla {
+static __device__ __align__(256) unsigned char g_static_scratch[MLA_STATIC_SCRATCH_BYTES];
+static void* g_static_ptr[64];
+static std::mutex g_static_mu;
+
+// Device address of g_static_scratch on the current device, looked up once per device (with
+// that device current) by the first call.
+static mla_status static_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return MLA_ERR_CUDA;
+        }
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return MLA_OK;
+}
+}  // namespace mla
+
+extern "C" {
+
+mla_status mla_decode_static(const mla_config* cfg, const mla_cache* cache, const void* q_cat,
+                             void* o_lat, float* lse, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    size_t need = 0;
+    if ((st = mla_workspace_size(cfg, &need)) != MLA_OK) return st;
+    if (need > MLA_STATIC_SCRATCH_BYTES) return MLA_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    if ((st = static_scratch(&scratch)) != MLA_OK) return st;
+    return mla_decode(cfg, cache, q_cat, o_lat, lse, scratch, MLA_STATIC_SCRATCH_BYTES, stream);
 }
 
 mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, int32_t seq,
