@@ -158,9 +158,23 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
         count_launches(1);
         g_last_path = 1;
     }
-    dim3 cgrid(qs.n_queries, (d_c / 4 + COMBINE_QUADS - 1) / COMBINE_QUADS);
-    if (cfg->dtype == MLA_BF16) combine_kernel<bf16><<<cgrid, 128, 0, stream>>>(a);
-    else combine_kernel<float><<<cgrid, 128, 0, stream>>>(a);
+    // the combine is a programmatic dependent of the attention kernel: it may start early and
+    // waits (griddepcontrol.wait) for the attention grid's results before reading partials
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(qs.n_queries, (unsigned)((n_h * (d_c / 4) + COMBINE_THREADS - 1) / COMBINE_THREADS));
+    lc.blockDim = dim3(COMBINE_THREADS);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t e = cfg->dtype == MLA_BF16 ? cudaLaunchKernelEx(&lc, combine_kernel<bf16>, a)
+                                           : cudaLaunchKernelEx(&lc, combine_kernel<float>, a);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
     count_launches(1);
     return launch_status();
 }
@@ -237,7 +251,7 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const
     g.seq_idx = seq_idx; g.pos = pos;
     g.page_table = cache->page_table; g.max_pages = cache->max_pages; g.batch = cache->batch;
     g.page_size = cfg->page_size; g.num_pages = cache->num_pages; g.width = W;
-    g.d_rope = cfg->d_rope; g.rope_base = cfg->rope_base;
+    rope_freq_fill(&g.rf, cfg->d_rope, cfg->rope_base);
     dim3 grid((W + 63) / 64, (n_tokens + 63) / 64, 1);
     if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_APPEND><<<grid, 256, 0, s>>>(g);
     else simt_gemm_kernel<float, EPI_APPEND><<<grid, 256, 0, s>>>(g);
@@ -278,10 +292,12 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
         if ((st = launch_status()) != MLA_OK) return st;
     }
     const dim3 blocks(n_tokens, (n_h + ROPE_HEADS - 1) / ROPE_HEADS);
+    RopeFreq rf;
+    rope_freq_fill(&rf, d_r, cfg->rope_base);
     if (cfg->dtype == MLA_BF16)
-        rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, cfg->rope_base);
+        rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, rf);
     else
-        rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, cfg->rope_base);
+        rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, rf);
     count_launches(1);
     return launch_status();
 }

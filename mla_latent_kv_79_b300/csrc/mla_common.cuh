@@ -1,6 +1,8 @@
 // Common device helpers for libmla: element types, the per-device error word, RoPE angles.
 #pragma once
 
+#include <cmath>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -26,15 +28,26 @@ template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
 
-// RoPE for interleaved pair i of a d_r-wide vector at position pos: angle = pos*base^(-2i/d_r),
-// evaluated in double so long positions keep full angle precision.
-__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d_r, float base, float* c, float* s) {
-    double theta = pow((double)base, -2.0 * (double)i / (double)d_r);
-    double ang = (double)pos * theta;
-    double sd, cd;
-    sincos(ang, &sd, &cd);
-    *c = (float)cd;
-    *s = (float)sd;
+// RoPE frequencies theta_i = base^(-2i/d_r) of the interleaved pairs (2i, 2i+1), evaluated in
+// double on the host and passed by value (d_r <= 1024).
+constexpr int MAX_ROPE_PAIRS = 512;
+struct RopeFreq {
+    double theta[MAX_ROPE_PAIRS];
+};
+
+inline void rope_freq_fill(RopeFreq* f, int d_r, float base) {
+    for (int i = 0; i < d_r / 2 && i < MAX_ROPE_PAIRS; ++i)
+        f->theta[i] = std::pow((double)base, -2.0 * (double)i / (double)d_r);
+}
+
+// cos and sin of the angle pos * theta.  The product and its reduction to [-pi, pi] are done
+// in double, so the angle keeps full precision at long positions; sin and cos of the reduced
+// angle are then taken in float (absolute error below 1e-6, far under bf16 rounding).
+__device__ __forceinline__ void rope_cos_sin(int pos, double theta, float* c, float* s) {
+    const double ang = (double)pos * theta;
+    const double k = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
+    const float r = (float)fma(-k, 6.283185307179586, ang);
+    sincosf(r, s, c);
 }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {

@@ -157,72 +157,94 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
 }
 
 // Log-sum-exp merge of the split partials of every split query; also writes the empty-query
-// result (o = 0, lse = -inf).  Grid (Q, ceil(d_c / 32)), 128 threads: a thread per head (loop
-// when n_h > 128), eight column quads per block, partial reads coalesced across heads.
-constexpr int COMBINE_QUADS = 8;
+// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h * d_c/4 / COMBINE_THREADS)): one thread per
+// (head, column quad), heads fastest, so a warp reads 512 contiguous bytes of a partial.  The
+// slots of a query are read in batches of COMBINE_BATCH independent loads with an online max,
+// i.e. one memory round trip per batch.  The schedule arithmetic reads only seq_lens, which the
+// attention kernel does not write, so it runs before the grid-dependency wait: launched as a
+// programmatic dependent, it overlaps the attention kernel's tail.
+constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_BATCH = 8;
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
     __shared__ long long red[SCHED_SCRATCH];
     const int q = blockIdx.x;
-    const int d_c = a.d_c;
-    const int quad0 = blockIdx.y * COMBINE_QUADS;
+    const int n_h = a.n_h, d_c = a.d_c;
     const int np = query_pages(a.qs, q);
-    const long long total = block_total_pages(a.qs, red);
+    // total pages and pages before q: one pass over seq_lens, two block sums
+    long long pq, total;
+    if (a.qs.mode == 1) {
+        pq = block_prefix_pages(a.qs, q, red);
+        total = block_prefix_pages(a.qs, a.qs.n_queries, red);
+    } else {
+        long long sq = 0, st = 0;
+        for (int i = threadIdx.x; i < a.qs.n_queries; i += blockDim.x) {
+            const int pi = query_pages(a.qs, i);
+            st += pi;
+            if (i < q) sq += pi;
+        }
+        pq = block_sum_ll(sq, red);
+        total = block_sum_ll(st, red);
+    }
     long long per = (total + a.n_units - 1) / a.n_units;
     if (per < 1) per = 1;
-    const long long pq = block_prefix_pages(a.qs, q, red);
     const long long u_lo = pq / per, u_hi = np > 0 ? (pq + np - 1) / per : u_lo;
     if (np > 0 && u_lo == u_hi) return;  // written directly by the attention kernel
-    auto slot_of = [&](long long u) { return (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1; };
-    for (int h = threadIdx.x; h < a.n_h; h += blockDim.x) {
-        T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * a.n_h + h) * d_c;
-        if (np == 0) {
-            for (int c = quad0 * 4; c < min(d_c, (quad0 + COMBINE_QUADS) * 4); ++c) out[c] = from_f32<T>(0.f);
-            if (blockIdx.y == 0) a.lse[(long long)q * a.n_h + h] = -INFINITY;
-            continue;
-        }
-        // slot weights once (independent loads), then for each slot eight independent
-        // float4 loads: the chain length is the number of slots, not slots x quads
-        const int ns = (int)(u_hi - u_lo + 1);
-        float mx = -INFINITY;
-        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, a.part_lse[slot_of(u_lo + i) * a.n_h + h]);
-        float wsum = 0.f;
-        for (int i = 0; i < ns; ++i) {
-            const float l = a.part_lse[slot_of(u_lo + i) * a.n_h + h];
-            wsum += (l == -INFINITY) ? 0.f : __expf(l - mx);
-        }
-        const float inv = 1.f / wsum;
-        const int nq = min(COMBINE_QUADS, d_c / 4 - quad0);
-        float4 acc[COMBINE_QUADS];
-#pragma unroll
-        for (int j = 0; j < COMBINE_QUADS; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < ns; ++i) {
-            const long long sl = slot_of(u_lo + i);
-            const float l = a.part_lse[sl * a.n_h + h];
-            const float w = (l == -INFINITY) ? 0.f : __expf(l - mx) * inv;
-            const float4* src = reinterpret_cast<const float4*>(a.part_o + part_index(sl, h, 4 * quad0, a.n_h, d_c));
-            float4 v[COMBINE_QUADS];
-#pragma unroll
-            for (int j = 0; j < COMBINE_QUADS; ++j) v[j] = j < nq ? src[(size_t)j * a.n_h] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < COMBINE_QUADS; ++j) {
-                acc[j].x = fmaf(w, v[j].x, acc[j].x); acc[j].y = fmaf(w, v[j].y, acc[j].y);
-                acc[j].z = fmaf(w, v[j].z, acc[j].z); acc[j].w = fmaf(w, v[j].w, acc[j].w);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < COMBINE_QUADS; ++j) {
-            if (j < nq) {
-                const int c = 4 * (quad0 + j);
-                out[c] = from_f32<T>(acc[j].x);
-                out[c + 1] = from_f32<T>(acc[j].y);
-                out[c + 2] = from_f32<T>(acc[j].z);
-                out[c + 3] = from_f32<T>(acc[j].w);
-            }
-        }
-        if (blockIdx.y == 0) a.lse[(long long)q * a.n_h + h] = mx + logf(wsum);
+
+    const int e = blockIdx.y * blockDim.x + threadIdx.x;
+    if (e >= n_h * (d_c / 4)) return;
+    const int h = e % n_h, quad = e / n_h;
+    T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * n_h + h) * d_c + 4 * quad;
+    if (np == 0) {
+        for (int j = 0; j < 4; ++j) out[j] = from_f32<T>(0.f);
+        if (quad == 0) a.lse[(long long)q * n_h + h] = -INFINITY;
+        return;
     }
+    grid_dependency_wait();  // partials of the attention kernel are complete and visible
+
+    auto slot_of = [&](long long u) { return (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1; };
+    const int ns = (int)(u_hi - u_lo + 1);
+    float mx = -INFINITY, wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < ns; i0 += COMBINE_BATCH) {
+        float lv[COMBINE_BATCH];
+        float4 v[COMBINE_BATCH];
+#pragma unroll
+        for (int j = 0; j < COMBINE_BATCH; ++j) {
+            lv[j] = -INFINITY;
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i0 + j < ns) {
+                const long long sl = slot_of(u_lo + i0 + j);
+                lv[j] = a.part_lse[sl * n_h + h];
+                v[j] = *reinterpret_cast<const float4*>(a.part_o + part_index(sl, h, 4 * quad, n_h, d_c));
+            }
+        }
+        float m_new = mx;
+#pragma unroll
+        for (int j = 0; j < COMBINE_BATCH; ++j) m_new = fmaxf(m_new, lv[j]);
+        if (m_new == -INFINITY) continue;
+        const float r = (mx == -INFINITY) ? 0.f : __expf(mx - m_new);
+        wsum *= r;
+        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+        for (int j = 0; j < COMBINE_BATCH; ++j) {
+            const float w = (lv[j] == -INFINITY) ? 0.f : __expf(lv[j] - m_new);
+            wsum += w;
+            acc.x = fmaf(w, v[j].x, acc.x); acc.y = fmaf(w, v[j].y, acc.y);
+            acc.z = fmaf(w, v[j].z, acc.z); acc.w = fmaf(w, v[j].w, acc.w);
+        }
+        mx = m_new;
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    out[0] = from_f32<T>(acc.x * inv);
+    out[1] = from_f32<T>(acc.y * inv);
+    out[2] = from_f32<T>(acc.z * inv);
+    out[3] = from_f32<T>(acc.w * inv);
+    if (quad == 0) a.lse[(long long)q * n_h + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 }  // namespace mla

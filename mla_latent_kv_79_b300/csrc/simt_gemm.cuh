@@ -25,7 +25,7 @@ struct SimtGemmArgs {
     const int* seq_idx; const int* pos;
     const int* page_table; int max_pages; int batch; int page_size; long long num_pages;
     int width;                           // W (row width of the pool)
-    int d_rope; float rope_base;
+    RopeFreq rf;                         // append: frequencies of the RoPE pairs
 };
 
 template <typename T, int EPI>
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs g) {
                 float v0 = acc[i][j], v1 = acc[i][j + 1];
                 if (n >= g.n_split && n < g.N) {
                     float c, s;
-                    rope_cos_sin(p, (n - g.n_split) / 2, g.d_rope, g.rope_base, &c, &s);
+                    rope_cos_sin(p, g.rf.theta[(n - g.n_split) / 2], &c, &s);
                     float r0 = v0 * c - v1 * s, r1 = v0 * s + v1 * c;
                     v0 = r0; v1 = r1;
                 }
@@ -127,20 +127,20 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemmArgs g) {
 }
 
 // RoPE part of the absorbed query: q_cat[n,h,d_c+2i : d_c+2i+2] = rotate(q_rope[n,h,2i:2i+2], pos[n]).
-// Grid (n_tokens, ceil(n_h / ROPE_HEADS)): the d_r/2 angles of the token are evaluated once per
-// block (double precision) into shared memory; each thread then rotates a few pairs.
+// Grid (n_tokens, ceil(n_h / ROPE_HEADS)): the d_r/2 (cos, sin) of the token are evaluated once
+// per block into shared memory; each thread then rotates a few pairs.
 constexpr int ROPE_HEADS = 16;
 
 template <typename T>
 __global__ void __launch_bounds__(256) rope_query_kernel(const T* __restrict__ q_rope, const int* __restrict__ pos,
                                                          T* __restrict__ q_cat, int n_tokens, int n_h, int d_r,
-                                                         int d_c, float base) {
+                                                         int d_c, const __grid_constant__ RopeFreq rf) {
     __shared__ float cs[512], sn[512];   // d_r <= 1024
     const int n = blockIdx.x;
     const int h0 = blockIdx.y * ROPE_HEADS;
     const int half = d_r / 2;
     const int p = __ldg(pos + n);
-    for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(p, i, d_r, base, &cs[i], &sn[i]);
+    for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(p, rf.theta[i], &cs[i], &sn[i]);
     __syncthreads();
     const int nh = min(ROPE_HEADS, n_h - h0);
     for (int e = threadIdx.x; e < nh * half; e += blockDim.x) {

@@ -439,6 +439,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     long long* red = reinterpret_cast<long long*>(smem + OFF_RED);
 
+    // the split combine (a programmatic dependent) may be scheduled now; it waits for this
+    // grid's completion before it reads anything this kernel writes
+    launch_dependents();
     const uint32_t rank = ptx::cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int unit = blockIdx.x >> 1;
