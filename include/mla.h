@@ -190,7 +190,10 @@ MLA_API mla_status mla_get_device_error(mla_stream_t stream);
 typedef enum {
     MLA_TUNE_ATTN_UNITS = 0,   /* >0: number of split units for decode/prefill (test use)    */
     MLA_TUNE_FORCE_SIMT = 1,   /* 1: run the portable SIMT kernels even where tcgen05 applies */
-    MLA_TUNE_WAIT_LIMIT_US = 2 /* device bounded-wait limit in microseconds (default 2e6)   */
+    MLA_TUNE_WAIT_LIMIT_US = 2, /* device bounded-wait limit in microseconds (default 2e6)  */
+    MLA_TUNE_GEMM_HEADS = 3,   /* >0: heads per CTA of the tcgen05 projection GEMMs          */
+    MLA_TUNE_GEMM_STAGES = 4,  /* >0: ring depth of the tcgen05 projection GEMMs             */
+    MLA_TUNE_NO_PDL = 5        /* 1: launch without programmatic dependent launch            */
 } mla_tuning_key;
 MLA_API int32_t mla_set_tuning(int32_t key, int32_t value);
 

@@ -38,6 +38,19 @@ static mla_status device_info(DeviceInfo** out) {
                 cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
                 return MLA_ERR_CUDA;
+            // one shared-memory carve-out for every kernel of the library, so consecutive
+            // launches of the hot path never wait for an SM to re-partition L1 and shared memory
+            const void* fns[] = {
+                (const void*)simt_gemm_kernel<bf16, EPI_STORE>, (const void*)simt_gemm_kernel<float, EPI_STORE>,
+                (const void*)simt_gemm_kernel<bf16, EPI_APPEND>, (const void*)simt_gemm_kernel<float, EPI_APPEND>,
+                (const void*)rope_query_kernel<bf16>, (const void*)rope_query_kernel<float>,
+                (const void*)simt_attention_kernel<bf16>, (const void*)simt_attention_kernel<float>,
+                (const void*)combine_kernel<bf16>, (const void*)combine_kernel<float>,
+                (const void*)tca::tc_attention_kernel, (const void*)tcg::tc_gemm_kernel};
+            for (const void* f : fns)
+                if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                    return MLA_ERR_CUDA;
             d.ready = true;
         }
     }
@@ -46,7 +59,7 @@ static mla_status device_info(DeviceInfo** out) {
 }
 
 // ----------------------------------------------------------------------------- knobs
-static std::atomic<int> g_tune[3] = {{0}, {0}, {2000000}};
+static std::atomic<int> g_tune[6] = {{0}, {0}, {2000000}, {0}, {0}, {0}};
 static thread_local int g_last_path = 0;
 static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 static std::atomic<unsigned long long> g_launches{0};
@@ -64,6 +77,7 @@ static mla_status check_config(const mla_config* c) {
         c->d_model <= 0 || c->page_size <= 0)
         return MLA_ERR_INVALID_ARG;
     if ((c->d_rope & 1) || (c->d_latent & 1)) return MLA_ERR_INVALID_ARG;
+    if (c->d_latent % 8) return MLA_ERR_UNSUPPORTED;  // 16-byte groups of the split partials
     if (!(c->rope_base > 0.f) || !std::isfinite(c->rope_base)) return MLA_ERR_INVALID_ARG;
     if (c->softmax_scale < 0.f || !std::isfinite(c->softmax_scale)) return MLA_ERR_INVALID_ARG;
     // row widths in bytes must keep 16-byte alignment of every row
@@ -93,6 +107,15 @@ static mla_status launch_status() {
 
 static int max_units(const DeviceInfo* d) { return d->sms > 0 ? d->sms : 148; }
 
+static tcg::Tuning gemm_tuning(unsigned long long wait_ns) {
+    tcg::Tuning t;
+    t.wait_ns = wait_ns;
+    t.hpc = g_tune[MLA_TUNE_GEMM_HEADS].load();
+    t.stages = g_tune[MLA_TUNE_GEMM_STAGES].load();
+    t.pdl = g_tune[MLA_TUNE_NO_PDL].load() == 0;
+    return t;
+}
+
 // ----------------------------------------------------------------------------- attention
 static mla_status attention(const mla_config* cfg, const mla_cache* cache, QuerySet qs,
                             const void* q_cat, void* o_lat, float* lse, void* ws, size_t ws_bytes,
@@ -118,8 +141,8 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
     a.num_pages = cache->num_pages;
     a.o_lat = o_lat;
     a.lse = lse;
-    a.part_o = reinterpret_cast<float*>(ws);
-    a.part_lse = a.part_o + (size_t)2 * U_max * n_h * d_c;
+    a.part_o = ws;  // partials sized as fp32 (an upper bound for either dtype), then the lse slots
+    a.part_lse = reinterpret_cast<float*>(ws) + (size_t)2 * U_max * n_h * d_c;
     a.n_h = n_h;
     a.d_c = d_c;
     a.width = W;
@@ -161,14 +184,15 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
     // the combine is a programmatic dependent of the attention kernel: it may start early and
     // waits (griddepcontrol.wait) for the attention grid's results before reading partials
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(qs.n_queries, (unsigned)((n_h * (d_c / 4) + COMBINE_THREADS - 1) / COMBINE_THREADS));
+    const int vec = cfg->dtype == MLA_BF16 ? 8 : 4;  // partial values per 16 bytes
+    lc.gridDim = dim3(qs.n_queries, (unsigned)((n_h * (d_c / vec) + COMBINE_THREADS - 1) / COMBINE_THREADS));
     lc.blockDim = dim3(COMBINE_THREADS);
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = g_tune[MLA_TUNE_NO_PDL].load() ? 0 : 1;
     cudaError_t e = cfg->dtype == MLA_BF16 ? cudaLaunchKernelEx(&lc, combine_kernel<bf16>, a)
                                            : cudaLaunchKernelEx(&lc, combine_kernel<float>, a);
     if (e != cudaSuccess) {
@@ -202,7 +226,7 @@ const char* mla_status_string(mla_status s) {
 }
 
 int32_t mla_set_tuning(int32_t key, int32_t value) {
-    if (key < 0 || key > 2) return -1;
+    if (key < 0 || key > 5) return -1;
     if (key == MLA_TUNE_WAIT_LIMIT_US && value <= 0) value = 2000000;
     return g_tune[key].exchange(value);
 }
@@ -274,9 +298,21 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
     const int W = d_c + d_r;
     DeviceInfo* dev;
     if ((st = device_info(&dev)) != MLA_OK) return st;
+    // RoPE half first: the GEMM that follows is its programmatic dependent, issues its weight
+    // loads at once and waits for the RoPE grid before loading q_nope, so the RoPE grid is
+    // complete whenever the GEMM is
+    const dim3 blocks(n_tokens, (n_h + ROPE_HEADS - 1) / ROPE_HEADS);
+    RopeFreq rf;
+    rope_freq_fill(&rf, d_r, cfg->rope_base);
+    if (cfg->dtype == MLA_BF16)
+        rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, rf);
+    else
+        rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, rf);
+    count_launches(1);
+    if ((st = launch_status()) != MLA_OK) return st;
     const unsigned long long wait_ns = (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull;
     if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_absorb_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
-        st = tc_gemm_absorb(cfg, q_nope, w_uk, q_cat, n_tokens, wait_ns, s);
+        st = tc_gemm_absorb(cfg, q_nope, w_uk, q_cat, n_tokens, gemm_tuning(wait_ns), s);
         if (st != MLA_OK) return st;
         count_launches(1);
     } else {
@@ -291,15 +327,7 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
         count_launches(1);
         if ((st = launch_status()) != MLA_OK) return st;
     }
-    const dim3 blocks(n_tokens, (n_h + ROPE_HEADS - 1) / ROPE_HEADS);
-    RopeFreq rf;
-    rope_freq_fill(&rf, d_r, cfg->rope_base);
-    if (cfg->dtype == MLA_BF16)
-        rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, rf);
-    else
-        rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, rf);
-    count_launches(1);
-    return launch_status();
+    return MLA_OK;
 }
 
 mla_status mla_decode(const mla_config* cfg, const mla_cache* cache, const void* q_cat,
@@ -400,7 +428,7 @@ mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, v
     if ((st = device_info(&dev)) != MLA_OK) return st;
     if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_out_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
         st = tc_gemm_out(cfg, o_lat, w_uv, o, n_tokens,
-                         (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull, s);
+                         gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull), s);
         if (st == MLA_OK) count_launches(1);
         return st;
     }

@@ -50,6 +50,13 @@ __device__ __forceinline__ void rope_cos_sin(int pos, double theta, float* c, fl
     sincosf(r, s, c);
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may
+// start before its predecessor ends; griddepcontrol.wait blocks the calling thread until the
+// predecessor grid has completed and its writes are visible.  launch_dependents lets the next
+// such kernel be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -19,7 +19,7 @@ struct AttnArgs {
     long long num_pages;
     void* o_lat;                // [Q, n_h, d_c] final output (dtype)
     float* lse;                 // [Q, n_h]
-    float* part_o;              // [2U, d_c/4, n_h, 4] fp32 partials (o / l), see part_index
+    void* part_o;               // [2U, d_c/V, n_h, V] partials (o / l) of the output dtype, see part_index
     float* part_lse;            // [2U, n_h]
     int n_units;
     int n_h, d_c, width;
@@ -28,10 +28,13 @@ struct AttnArgs {
 
 constexpr int SIMT_TB = 32;     // tokens per staged block
 
-// Split partials are stored head-contiguous per column quad, [slot][c/4][h][c%4], so that a
-// warp of consecutive heads writes (and the combine reads) contiguous memory.
+// Split partials are stored in the output dtype T, head-contiguous per 16-byte column group:
+// [slot][c/V][h][c%V] with V = 16 / sizeof(T), so that a warp of consecutive heads writes (and
+// the combine reads) contiguous memory.  d_c is a multiple of 8.
+template <typename T>
 __device__ __forceinline__ size_t part_index(long long slot, int h, int c, int n_h, int d_c) {
-    return (((size_t)slot * (d_c / 4) + (c >> 2)) * n_h + h) * 4 + (c & 3);
+    constexpr int V = 16 / sizeof(T);
+    return (((size_t)slot * (d_c / V) + (c / V)) * n_h + h) * V + (c % V);
 }
 
 __host__ __device__ inline size_t simt_attn_smem_bytes(int hg, int width, int d_c) {
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
             if (sg.direct)
                 reinterpret_cast<T*>(a.o_lat)[((long long)sg.q * a.n_h + h0 + h) * d_c + c] = from_f32<T>(v);
             else
-                a.part_o[part_index(sg.slot, h0 + h, c, a.n_h, d_c)] = v;
+                reinterpret_cast<T*>(a.part_o)[part_index<T>(sg.slot, h0 + h, c, a.n_h, d_c)] = from_f32<T>(v);
         }
         for (int h = tid; h < nh_here; h += blockDim.x) {
             float l = l_s[h];
@@ -157,21 +160,52 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
 }
 
 // Log-sum-exp merge of the split partials of every split query; also writes the empty-query
-// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h * d_c/4 / COMBINE_THREADS)): one thread per
-// (head, column quad), heads fastest, so a warp reads 512 contiguous bytes of a partial.  The
-// slots of a query are read in batches of COMBINE_BATCH independent loads with an online max,
-// i.e. one memory round trip per batch.  The schedule arithmetic reads only seq_lens, which the
-// attention kernel does not write, so it runs before the grid-dependency wait: launched as a
-// programmatic dependent, it overlaps the attention kernel's tail.
+// result (o = 0, lse = -inf).  Grid (Q, ceil(n_h * d_c/V / COMBINE_THREADS)): one thread per
+// (head, 16-byte column group of V values), heads fastest, so a warp reads 512 contiguous
+// bytes of a partial.  The slots of a query are read in batches of COMBINE_BATCH independent
+// loads with an online max, i.e. one memory round trip per batch.  The schedule arithmetic
+// reads only seq_lens, which the attention kernel does not write, so it runs before the
+// grid-dependency wait: launched as a programmatic dependent, it overlaps the attention
+// kernel's tail.
 constexpr int COMBINE_THREADS = 256;
 constexpr int COMBINE_BATCH = 8;
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& u, float* f) {
+    if constexpr (sizeof(T) == 4) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    } else {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float* f) {
+    uint4 u;
+    if constexpr (sizeof(T) == 4) {
+        u.x = __float_as_uint(f[0]); u.y = __float_as_uint(f[1]); u.z = __float_as_uint(f[2]); u.w = __float_as_uint(f[3]);
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        u.x = w[0]; u.y = w[1]; u.z = w[2]; u.w = w[3];
+    }
+    return u;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
+    constexpr int V = 16 / sizeof(T);
     __shared__ long long red[SCHED_SCRATCH];
+    launch_dependents();  // the output projection may stage its weights meanwhile
     const int q = blockIdx.x;
     const int n_h = a.n_h, d_c = a.d_c;
     const int np = query_pages(a.qs, q);
@@ -196,12 +230,12 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
     if (np > 0 && u_lo == u_hi) return;  // written directly by the attention kernel
 
     const int e = blockIdx.y * blockDim.x + threadIdx.x;
-    if (e >= n_h * (d_c / 4)) return;
-    const int h = e % n_h, quad = e / n_h;
-    T* out = reinterpret_cast<T*>(a.o_lat) + ((long long)q * n_h + h) * d_c + 4 * quad;
+    if (e >= n_h * (d_c / V)) return;
+    const int h = e % n_h, grp = e / n_h;
+    uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.o_lat) + ((long long)q * n_h + h) * d_c + V * grp);
     if (np == 0) {
-        for (int j = 0; j < 4; ++j) out[j] = from_f32<T>(0.f);
-        if (quad == 0) a.lse[(long long)q * n_h + h] = -INFINITY;
+        *out = make_uint4(0u, 0u, 0u, 0u);
+        if (grp == 0) a.lse[(long long)q * n_h + h] = -INFINITY;
         return;
     }
     grid_dependency_wait();  // partials of the attention kernel are complete and visible
@@ -209,18 +243,21 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
     auto slot_of = [&](long long u) { return (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1; };
     const int ns = (int)(u_hi - u_lo + 1);
     float mx = -INFINITY, wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+    const T* po = reinterpret_cast<const T*>(a.part_o);
     for (int i0 = 0; i0 < ns; i0 += COMBINE_BATCH) {
         float lv[COMBINE_BATCH];
-        float4 v[COMBINE_BATCH];
+        uint4 v[COMBINE_BATCH];
 #pragma unroll
         for (int j = 0; j < COMBINE_BATCH; ++j) {
             lv[j] = -INFINITY;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
             if (i0 + j < ns) {
                 const long long sl = slot_of(u_lo + i0 + j);
                 lv[j] = a.part_lse[sl * n_h + h];
-                v[j] = *reinterpret_cast<const float4*>(a.part_o + part_index(sl, h, 4 * quad, n_h, d_c));
+                v[j] = *reinterpret_cast<const uint4*>(po + part_index<T>(sl, h, V * grp, n_h, d_c));
             }
         }
         float m_new = mx;
@@ -229,22 +266,24 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
         if (m_new == -INFINITY) continue;
         const float r = (mx == -INFINITY) ? 0.f : __expf(mx - m_new);
         wsum *= r;
-        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[c] *= r;
 #pragma unroll
         for (int j = 0; j < COMBINE_BATCH; ++j) {
             const float w = (lv[j] == -INFINITY) ? 0.f : __expf(lv[j] - m_new);
             wsum += w;
-            acc.x = fmaf(w, v[j].x, acc.x); acc.y = fmaf(w, v[j].y, acc.y);
-            acc.z = fmaf(w, v[j].z, acc.z); acc.w = fmaf(w, v[j].w, acc.w);
+            float f[V];
+            unpack16<T>(v[j], f);
+#pragma unroll
+            for (int c = 0; c < V; ++c) acc[c] = fmaf(w, f[c], acc[c]);
         }
         mx = m_new;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    out[0] = from_f32<T>(acc.x * inv);
-    out[1] = from_f32<T>(acc.y * inv);
-    out[2] = from_f32<T>(acc.z * inv);
-    out[3] = from_f32<T>(acc.w * inv);
-    if (quad == 0) a.lse[(long long)q * n_h + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[c] *= inv;
+    *out = pack16<T>(acc);
+    if (grp == 0) a.lse[(long long)q * n_h + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 }  // namespace mla

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(256) rope_query_kernel(const T* __restrict__ q
                                                          T* __restrict__ q_cat, int n_tokens, int n_h, int d_r,
                                                          int d_c, const __grid_constant__ RopeFreq rf) {
     __shared__ float cs[512], sn[512];   // d_r <= 1024
+    launch_dependents();  // the absorption GEMM writes the other columns of q_cat
     const int n = blockIdx.x;
     const int h0 = blockIdx.y * ROPE_HEADS;
     const int half = d_r / 2;

@@ -394,29 +394,41 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         }
         ptx::tc_fence_after();
         const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
-        for (int k = 0; k < 16; ++k) {
-            uint32_t r[32];
-            ptx::tmem_ld32(tO + 32 * k, r);
-            ptx::tmem_wait_ld();
-            if (sg.direct) {
-                uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(a.o_lat) + ((size_t)sg.q * NH + h) * DC +
-                                                     32 * k);
+        // bf16 rows of O / l: the final output row, or the partial layout [slot][c/8][h][8]
+        // in which a warp's 32 heads write 512 contiguous bytes.  The TMEM load of the next
+        // 32 columns is in flight while the current ones are converted and stored.
+        uint4* dst;
+        size_t step;
+        if (sg.direct) {
+            dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(a.o_lat) + ((size_t)sg.q * NH + h) * DC);
+            step = 1;
+        } else {
+            dst = reinterpret_cast<uint4*>(a.part_o) + (size_t)sg.slot * (DC / 8) * NH + h;
+            step = NH;
+        }
+        auto emit = [&](const uint32_t* r, int k) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint4 v;
-                    v.x = ptx::pack_bf16(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-                    v.y = ptx::pack_bf16(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-                    v.z = ptx::pack_bf16(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-                    v.w = ptx::pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-                    d4[i] = v;
-                }
-            } else {
-                // partial layout [slot][c/4][h][c%4]: a warp's 32 heads write 512 contiguous bytes
-                float4* d4 = reinterpret_cast<float4*>(a.part_o) + ((size_t)sg.slot * (DC / 4) + 8 * k) * NH + h;
+            for (int i = 0; i < 4; ++i) {
+                uint4 v;
+                v.x = ptx::pack_bf16(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+                v.y = ptx::pack_bf16(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+                v.z = ptx::pack_bf16(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+                v.w = ptx::pack_bf16(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+                dst[(size_t)(4 * k + i) * step] = v;
+            }
+        };
+        {
+            uint32_t ra[32], rb[32];
+            ptx::tmem_ld32(tO, ra);
+            ptx::tmem_wait_ld_regs(ra);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    d4[(size_t)i * NH] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                                     __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+            for (int k = 0; k < 16; k += 2) {
+                ptx::tmem_ld32(tO + 32 * (k + 1), rb);
+                emit(ra, k);
+                ptx::tmem_wait_ld_regs(rb);
+                if (k + 2 < 16) ptx::tmem_ld32(tO + 32 * (k + 2), ra);
+                emit(rb, k + 1);
+                if (k + 2 < 16) ptx::tmem_wait_ld_regs(ra);
             }
         }
         ptx::tc_fence_before();
@@ -442,6 +454,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // the split combine (a programmatic dependent) may be scheduled now; it waits for this
     // grid's completion before it reads anything this kernel writes
     launch_dependents();
+    // the schedule reads seq_lens first: start those lines towards L1 before the set-up below
+    if (a.qs.mode == 0 && threadIdx.x * 32 < a.qs.n_queries)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.qs.seq_lens + threadIdx.x * 32));
     const uint32_t rank = ptx::cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int unit = blockIdx.x >> 1;

@@ -5,10 +5,12 @@
 //
 // Both are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
 // 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, as the weight is stored) and
-// up to 256 tokens as B (K-major).  With few tokens (decode) the tile streams the weights
-// once at HBM speed; with many (prefill) the grid tiles the tokens.  Each CTA owns one
-// (m-tile, head, n-tile): warp 0 TMA-loads 64-wide K chunks of A and B into a 4-stage ring,
-// warp 1 issues the MMAs into TMEM, warps 2-5 drain D (one row per thread).
+// up to 256 tokens as B (K-major).  Each CTA owns one m-tile of up to HPC heads for one n-tile:
+// warp 0 streams 64-wide K chunks of A and B through a ring that fills shared memory, warp 1
+// issues the MMAs into one TMEM accumulator per head, warps 2-5 drain D (one row per thread).
+// With few tokens (decode) a CTA's whole weight slice is in flight at once.  The kernel is
+// launched as a programmatic dependent: the weights do not depend on the previous kernel, so
+// their loads are issued before the grid-dependency wait and only the token operand after it.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -18,17 +20,35 @@
 namespace mla {
 namespace tcg {
 
-constexpr int BM = 128, BK = 64, MAX_N = 256, STAGES = 4;
+constexpr int BM = 128, BK = 64, MAX_N = 256, HPC = 4, MAX_STAGES = 16;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int NTHREADS = 192;
+constexpr int SMEM_LIMIT = 232448;            // opt-in shared memory per CTA
 
 // stage = A tile + B tile (n_pad rows of 128 B), rounded to the 1 KB swizzle atom
 __host__ __device__ inline int stage_bytes(int n_pad) { return (A_BYTES + n_pad * BK * 2 + 1023) & ~1023; }
-__host__ __device__ inline int smem_bytes(int n_pad) { return STAGES * stage_bytes(n_pad) + 128; }
+__host__ __device__ inline int smem_bytes(int n_pad, int stages) { return stages * stage_bytes(n_pad) + 16 * stages + 32; }
 __host__ __device__ inline uint32_t tmem_cols(int n_pad) {
     uint32_t c = 32;
     while ((int)c < n_pad) c <<= 1;
     return c;
+}
+// Ring depth.  Few tokens: three stages, so that four CTAs share an SM (measured on B300: the
+// weight streams gain from more resident CTAs, not from a deeper ring per CTA).  Many tokens:
+// as deep as shared memory allows.
+inline int max_stages(int n_pad) {
+    int s = (SMEM_LIMIT - 32) / (stage_bytes(n_pad) + 16);
+    return s < MAX_STAGES ? s : MAX_STAGES;
+}
+inline int stages_for(int n_pad) {
+    const int s = max_stages(n_pad);
+    return n_pad <= 64 && s > 3 ? 3 : s;
+}
+// Heads per CTA (one TMEM accumulator of tmem_cols(n_pad) columns each, <= 512 columns in all).
+// One by default: more CTAs stream the weights faster than fewer CTAs with more heads each.
+inline int max_heads_per_cta(int n_pad) {
+    int h = 512 / (int)tmem_cols(n_pad);
+    return h < HPC ? h : HPC;
 }
 
 enum Mode { ABSORB = 0, OUT = 1 };
@@ -39,8 +59,17 @@ struct GemmArgs {
     int n_pad;          // MMA N (multiple of 16, >= 16, <= 256)
     int k_chunks;       // K / 64
     int n_h, d_h, d_c, width;
+    int stages;         // ring depth
+    int hpc;            // heads per CTA
     void* out;          // q_cat (ABSORB) or o (OUT), bf16
     unsigned long long wait_ns;
+};
+
+// launch choices (0 = automatic), from the library's tuning knobs
+struct Tuning {
+    unsigned long long wait_ns = 2000000000ull;
+    int hpc = 0, stages = 0;
+    bool pdl = true;
 };
 
 __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned long long limit) {
@@ -58,7 +87,17 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned lo
     }
 }
 
-// grid: (m-tiles, n_h, n-tiles)
+// Chunk c of a CTA with nh heads: head-major for ABSORB (a head's K chunks are adjacent columns
+// of W_UK), K-major for OUT (the CTA's heads are adjacent column slabs of W_UV, so one 64-row
+// block of all of them is requested together).
+__device__ __forceinline__ int chunk_head(const GemmArgs& g, int c, int nh) {
+    return g.mode == OUT ? c % nh : c / g.k_chunks;
+}
+__device__ __forceinline__ int chunk_k(const GemmArgs& g, int c, int nh) {
+    return g.mode == OUT ? c / nh : c % g.k_chunks;
+}
+
+// grid: (m-tiles, ceil(n_h / hpc), n-tiles)
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -68,15 +107,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * MAX_N;
-    const int SB = stage_bytes(g.n_pad);
-    const uint32_t ncols = tmem_cols(g.n_pad);
-    const uint32_t bar_full = base + STAGES * SB, bar_empty = bar_full + 8 * STAGES, bar_done = bar_empty + 8 * STAGES;
+    const int mt = blockIdx.x, h0 = blockIdx.y * g.hpc, n0 = blockIdx.z * MAX_N;
+    const int nh = min(g.hpc, g.n_h - h0);
+    const int S = g.stages, SB = stage_bytes(g.n_pad);
+    const uint32_t acc_cols = tmem_cols(g.n_pad);                  // columns per head accumulator
+    const uint32_t ncols = tmem_cols((int)acc_cols * g.hpc);
+    const uint32_t bar_full = base + S * SB, bar_empty = bar_full + 8 * S, bar_done = bar_empty + 8 * S;
     const uint32_t slot = bar_done + 8;
     const bool a_mn = g.mode == OUT;
+    const int total = nh * g.k_chunks;                             // chunks of this CTA, head-major
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
             ptx::mbar_init(bar_empty + 8 * s, 1);
         }
@@ -95,42 +137,57 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem + (slot - base));
-    bool ok = true;
 
     if (warp == 0 && lane == 0) {
         const uint32_t bytes = (uint32_t)(A_BYTES + g.n_pad * BK * 2);
-        for (int kc = 0; kc < g.k_chunks; ++kc) {
-            const int s = kc % STAGES;
-            if (!gwait(bar_empty + 8 * s, ((kc / STAGES) & 1u) ^ 1u, g.wait_ns)) { ok = false; break; }
-            const uint32_t st = base + s * SB, fb = bar_full + 8 * s;
-            ptx::mbar_arrive_expect_tx(fb, bytes);
+        auto load_a = [&](int c, uint32_t st, uint32_t fb) {
+            const int h = h0 + chunk_head(g, c, nh), kc = chunk_k(g, c, nh);
             if (g.mode == ABSORB) {
-                // A: W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
+                // W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + kc * BK, mt * BM, fb);
-                // B: q_nope viewed [n, n_h*d_h]: cols h*d_h + kc*64, rows n0 .. n0 + n_pad
-                ptx::tma_load_2d(st + A_BYTES, &tmB, h * g.d_h + kc * BK, n0, fb);
             } else {
-                // A: W_UV rows c in [kc*64, +64) x cols h*d_h + mt*128 + {0, 64} (MN-major, two boxes)
+                // W_UV rows c in [kc*64, +64) x cols h*d_h + mt*128 + {0, 64} (MN-major, two boxes)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + mt * BM, kc * BK, fb);
                 ptx::tma_load_2d(st + BK * 128, &tmA, h * g.d_h + mt * BM + 64, kc * BK, fb);
-                // B: o_lat viewed [n, n_h*d_c]: cols h*d_c + kc*64
-                ptx::tma_load_2d(st + A_BYTES, &tmB, h * g.d_c + kc * BK, n0, fb);
             }
+        };
+        auto load_b = [&](int c, uint32_t st, uint32_t fb) {
+            const int h = h0 + chunk_head(g, c, nh), kc = chunk_k(g, c, nh);
+            // q_nope viewed [n, n_h*d_h] (ABSORB) or o_lat viewed [n, n_h*d_c] (OUT)
+            const int col = (g.mode == ABSORB ? h * g.d_h : h * g.d_c) + kc * BK;
+            ptx::tma_load_2d(st + A_BYTES, &tmB, col, n0, fb);
+        };
+        // the first ring's worth of weights goes out before the previous kernel has finished
+        const int pre = total < S ? total : S;
+        for (int c = 0; c < pre; ++c) {
+            ptx::mbar_arrive_expect_tx(bar_full + 8 * c, bytes);
+            load_a(c, base + c * SB, bar_full + 8 * c);
+        }
+        grid_dependency_wait();
+        for (int c = 0; c < pre; ++c) load_b(c, base + c * SB, bar_full + 8 * c);
+        for (int c = pre; c < total; ++c) {
+            const int s = c % S;
+            if (!gwait(bar_empty + 8 * s, ((c / S) & 1u) ^ 1u, g.wait_ns)) break;
+            const uint32_t st = base + s * SB, fb = bar_full + 8 * s;
+            ptx::mbar_arrive_expect_tx(fb, bytes);
+            load_a(c, st, fb);
+            load_b(c, st, fb);
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t idesc = ptx::idesc_bf16(BM, g.n_pad, a_mn, false);
-        for (int kc = 0; kc < g.k_chunks; ++kc) {
-            const int s = kc % STAGES;
-            if (!gwait(bar_full + 8 * s, (kc / STAGES) & 1u, g.wait_ns)) { ok = false; break; }
+        for (int c = 0; c < total; ++c) {
+            const int s = c % S, kc = chunk_k(g, c, nh);
+            if (!gwait(bar_full + 8 * s, (c / S) & 1u, g.wait_ns)) break;
             ptx::tc_fence_after();
             const uint32_t st = base + s * SB;
+            const uint32_t d = tmem + (uint32_t)chunk_head(g, c, nh) * acc_cols;
             const uint64_t da = a_mn ? ptx::desc_sw128(st, BK * 128, 1024) : ptx::desc_sw128(st, 16, 1024);
             const uint64_t db = ptx::desc_sw128(st + A_BYTES, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 // K-major A: +32 B per 16-wide K step; MN-major A: +16 rows of 128 B
                 const uint64_t a_off = a_mn ? (uint64_t)((kk * 2048) >> 4) : (uint64_t)((kk * 32) >> 4);
-                ptx::mma_ss(tmem, da + a_off, db + (uint64_t)((kk * 32) >> 4), idesc, (kc | kk) ? 1u : 0u);
+                ptx::mma_ss(d, da + a_off, db + (uint64_t)((kk * 32) >> 4), idesc, (kc | kk) ? 1u : 0u);
             }
             ptx::tc_commit(bar_empty + 8 * s);
         }
@@ -140,21 +197,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int row = qd * 32 + lane;  // m within the tile
         if (gwait(bar_done, 0, g.wait_ns)) {
             ptx::tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
             bf16* out = reinterpret_cast<bf16*>(g.out);
-            for (int c0 = 0; c0 < g.n_pad; c0 += 32) {  // reads stay inside the allocation (>= 32 columns)
-                uint32_t r[32];
-                ptx::tmem_ld32(taddr + c0, r);
-                ptx::tmem_wait_ld();
+            for (int j = 0; j < nh; ++j) {
+                const int h = h0 + j;
+                const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)j * acc_cols;
+                for (int c0 = 0; c0 < g.n_pad; c0 += 32) {  // reads stay inside the allocation (>= 32 columns)
+                    uint32_t r[32];
+                    ptx::tmem_ld32(taddr + c0, r);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = n0 + c0 + j;
-                    if (c0 + j < g.n_pad && n < g.n_tokens) {
-                        const bf16 v = __float2bfloat16_rn(__uint_as_float(r[j]));
-                        if (g.mode == ABSORB)
-                            out[((size_t)n * g.n_h + h) * g.width + mt * BM + row] = v;
-                        else
-                            out[(size_t)n * g.n_h * g.d_h + (size_t)h * g.d_h + mt * BM + row] = v;
+                    for (int i = 0; i < 32; ++i) {
+                        const int n = n0 + c0 + i;
+                        if (c0 + i < g.n_pad && n < g.n_tokens) {
+                            const bf16 v = __float2bfloat16_rn(__uint_as_float(r[i]));
+                            if (g.mode == ABSORB)
+                                out[((size_t)n * g.n_h + h) * g.width + mt * BM + row] = v;
+                            else
+                                out[(size_t)n * g.n_h * g.d_h + (size_t)h * g.d_h + mt * BM + row] = v;
+                        }
                     }
                 }
             }
@@ -197,14 +257,31 @@ inline int n_pad_for(int n) {
 }
 
 inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtensorMap& b, int m_tiles, int n_h,
-                         cudaStream_t stream) {
+                         const Tuning& t, cudaStream_t stream) {
     GemmArgs g = g0;
-    const int smem = smem_bytes(g.n_pad);
+    g.wait_ns = t.wait_ns;
+    g.stages = stages_for(g.n_pad);
+    if (t.stages > 0) g.stages = t.stages < max_stages(g.n_pad) ? t.stages : max_stages(g.n_pad);
+    g.hpc = 1;
+    if (t.hpc > 0) g.hpc = t.hpc < max_heads_per_cta(g.n_pad) ? t.hpc : max_heads_per_cta(g.n_pad);
+    const int smem = smem_bytes(g.n_pad, g.stages);
     if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return MLA_ERR_CUDA;
-    dim3 grid(m_tiles, n_h, (g.n_tokens + MAX_N - 1) / MAX_N);
-    tc_gemm_kernel<<<grid, NTHREADS, smem, stream>>>(a, b, g);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(m_tiles, (n_h + g.hpc - 1) / g.hpc, (g.n_tokens + MAX_N - 1) / MAX_N);
+    lc.blockDim = dim3(NTHREADS);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = t.pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&lc, tc_gemm_kernel, a, b, g) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    return MLA_OK;
 }
 
 }  // namespace tcg
@@ -220,7 +297,7 @@ inline bool tc_gemm_out_supported(const mla_config* c, int n, int cc_major, int 
 
 // q_cat[:, :, 0:d_c] of mla_absorb_q (the RoPE half is written by rope_query_kernel)
 inline mla_status tc_gemm_absorb(const mla_config* c, const void* q_nope, const void* w_uk, void* q_cat, int n,
-                                 unsigned long long wait_ns, cudaStream_t stream) {
+                                 const tcg::Tuning& t, cudaStream_t stream) {
     tcg::GemmArgs g{};
     g.mode = tcg::ABSORB;
     g.n_tokens = n;
@@ -228,17 +305,16 @@ inline mla_status tc_gemm_absorb(const mla_config* c, const void* q_nope, const 
     g.k_chunks = c->d_nope / tcg::BK;
     g.n_h = c->n_heads; g.d_h = c->d_nope; g.d_c = c->d_latent; g.width = c->d_latent + c->d_rope;
     g.out = q_cat;
-    g.wait_ns = wait_ns;
     const uint64_t hd = (uint64_t)c->n_heads * c->d_nope;
     CUtensorMap ta, tb;
     if (!tcg::encode_2d(&ta, w_uk, hd, (uint64_t)c->d_latent, hd, tcg::BM) ||
         !tcg::encode_2d(&tb, q_nope, hd, (uint64_t)n, hd, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
-    return tcg::launch(g, ta, tb, c->d_latent / tcg::BM, c->n_heads, stream);
+    return tcg::launch(g, ta, tb, c->d_latent / tcg::BM, c->n_heads, t, stream);
 }
 
 inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void* w_uv, void* o, int n,
-                              unsigned long long wait_ns, cudaStream_t stream) {
+                              const tcg::Tuning& t, cudaStream_t stream) {
     tcg::GemmArgs g{};
     g.mode = tcg::OUT;
     g.n_tokens = n;
@@ -246,13 +322,12 @@ inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void
     g.k_chunks = c->d_latent / tcg::BK;
     g.n_h = c->n_heads; g.d_h = c->d_nope; g.d_c = c->d_latent; g.width = c->d_latent + c->d_rope;
     g.out = o;
-    g.wait_ns = wait_ns;
     const uint64_t hd = (uint64_t)c->n_heads * c->d_nope, hc = (uint64_t)c->n_heads * c->d_latent;
     CUtensorMap ta, tb;
     if (!tcg::encode_2d(&ta, w_uv, hd, (uint64_t)c->d_latent, hd, 64) ||
         !tcg::encode_2d(&tb, o_lat, hc, (uint64_t)n, hc, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
-    return tcg::launch(g, ta, tb, c->d_nope / tcg::BM, c->n_heads, stream);
+    return tcg::launch(g, ta, tb, c->d_nope / tcg::BM, c->n_heads, t, stream);
 }
 
 }  // namespace mla

@@ -46,7 +46,7 @@ def test_nothing_else_is_exported(lib):
 
 def test_version_and_strings(lib):
     assert lib.mla_abi_version() == 1
-    for code in range(7):
+    for code in range(8):
         assert lib.mla_status_string(code)
     assert lib.mla_status_string(99) == b"unknown status"
 
