@@ -66,15 +66,24 @@ def source_digest():
 
 
 def ncu_traffic(kernel_key: str, workload: str):
-    """DRAM traffic per launch from a committed ncu summary, or None when the kernel sources
-    changed since that capture."""
-    p = os.path.join(PROFILE_DIR, f"{kernel_key}_{workload}.json")
+    """DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed
+    ncu summary profiles/<kernel>_<workload>.md, or None when it is missing or the kernel
+    sources changed since that capture (the summary records their digest)."""
+    p = os.path.join(PROFILE_DIR, f"{kernel_key}_{workload}.md")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    if d.get("source_digest") != source_digest():
+    fields = {}
+    for line in open(p):
+        line = line.strip().lstrip("-").strip()
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip().strip("`")] = v.strip().strip("`")
+    if fields.get("source_digest") != source_digest():
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
