@@ -86,6 +86,21 @@ def ncu_traffic(kernel_key: str, workload: str):
         return None
 
 
+def job_throughput(local_ms: float, local_units: int, device="cpu"):
+    """Whole-job throughput over all ranks of the default process group (or this process
+    alone): units summed over ranks divided by the slowest rank's time.
+    Returns (units per second, max ms over ranks, total units)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([int(local_units)], dtype=torch.int64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    ms, units = float(t.item()), int(u.item())
+    return units / (ms * 1e-3), ms, units
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -271,11 +286,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    value, total_ms, tokens_total = job_throughput(sum(step_ms), B * K, "cuda")
     path = M.mla_last_attention_path()
     assert M.mla_get_device_error() == 0
 
@@ -300,11 +311,8 @@ def run_ours(args):
         eev[i][1].record(stream)
     torch.cuda.synchronize()
     clock = clocks.stop()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+    e2e_value, e2e_ms, _ = job_throughput(sum(a.elapsed_time(b) for a, b in eev), B * K, "cuda")
     if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
         dist.barrier()
 
     if rank != 0:
@@ -316,10 +324,9 @@ def run_ours(args):
     k_mean_s = (sum(kern_ms) / K) * 1e-3
     achieved = alg_bytes / k_mean_s / 1e9
     kernel_key = "tc_attention" if path == 2 else "simt_attention"
-    tokens_total = B * K * world
     line = {
         "metric": METRIC,
-        "value": tokens_total / (total_ms * 1e-3),
+        "value": value,
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,
@@ -338,7 +345,7 @@ def run_ours(args):
                      "tflops": alg_flops / k_mean_s / 1e12, "peak_source": src,
                      "tensor_frac": alg_flops / k_mean_s / 1e12 / tflops,
                      "roofline_us": 1e6 * max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12))},
-        "e2e": {"value": tokens_total / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size()),
                 "d2h_bytes_per_step": int(h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size())},
         "gpu_launches": int(launches),
