@@ -274,15 +274,22 @@ def run_ours(args):
     launches0 = lib.mla_kernel_launches()
     for i in range(K):
         flush.zero_()
-        lib.mla_set_attention_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
-    lib.mla_set_attention_events(None, None)
     torch.cuda.synchronize()
     launches = lib.mla_kernel_launches() - launches0
     if world > 1:
         dist.barrier()
+    torch.cuda.synchronize()
+    # the attention kernel's own duration, from events the library records around its launch
+    # on the same stream; a separate pass, because events between two kernels keep the second
+    # from starting early (programmatic dependent launch) and would slow the timed steps
+    for i in range(K):
+        flush.zero_()
+        lib.mla_set_attention_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+        step()
+    lib.mla_set_attention_events(None, None)
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]

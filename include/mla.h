@@ -193,7 +193,8 @@ typedef enum {
     MLA_TUNE_WAIT_LIMIT_US = 2, /* device bounded-wait limit in microseconds (default 2e6)  */
     MLA_TUNE_GEMM_HEADS = 3,   /* >0: heads per CTA of the tcgen05 projection GEMMs          */
     MLA_TUNE_GEMM_STAGES = 4,  /* >0: ring depth of the tcgen05 projection GEMMs             */
-    MLA_TUNE_NO_PDL = 5        /* 1: launch without programmatic dependent launch            */
+    MLA_TUNE_NO_PDL = 5,       /* 1: launch without programmatic dependent launch            */
+    MLA_TUNE_SCHEDULE = 6      /* split schedule: 0 automatic, 1 flat page partition only     */
 } mla_tuning_key;
 MLA_API int32_t mla_set_tuning(int32_t key, int32_t value);
 

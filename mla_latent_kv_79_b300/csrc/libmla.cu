@@ -59,7 +59,7 @@ static mla_status device_info(DeviceInfo** out) {
 }
 
 // ----------------------------------------------------------------------------- knobs
-static std::atomic<int> g_tune[6] = {{0}, {0}, {2000000}, {0}, {0}, {0}};
+static std::atomic<int> g_tune[7] = {{0}, {0}, {2000000}, {0}, {0}, {0}, {0}};
 static thread_local int g_last_path = 0;
 static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 static std::atomic<unsigned long long> g_launches{0};
@@ -147,6 +147,7 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
     a.d_c = d_c;
     a.width = W;
     a.scale = scale_of(cfg);
+    a.qs.flat_only = g_tune[MLA_TUNE_SCHEDULE].load() == 1 ? 1 : 0;
 
     const int forced = g_tune[MLA_TUNE_ATTN_UNITS].load();
     const bool use_tc = !g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_attention_supported(cfg, cache, dev->cc_major, dev->cc_minor);
@@ -155,7 +156,8 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
         int U = forced > 0 ? (forced < U_max / 2 ? forced : U_max / 2) : U_max / 2;
         a.n_units = U;
         if (timed) cudaEventRecord(g_ev_before, stream);
-        st = tc_attention_launch(a, cache, (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull, stream);
+        st = tc_attention_launch(a, cache, (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull,
+                                 g_tune[MLA_TUNE_NO_PDL].load() == 0, stream);
         if (timed) cudaEventRecord(g_ev_after, stream);
         if (st != MLA_OK) return st;
         count_launches(1);
@@ -226,7 +228,7 @@ const char* mla_status_string(mla_status s) {
 }
 
 int32_t mla_set_tuning(int32_t key, int32_t value) {
-    if (key < 0 || key > 5) return -1;
+    if (key < 0 || key > 6) return -1;
     if (key == MLA_TUNE_WAIT_LIMIT_US && value <= 0) value = 2000000;
     return g_tune[key].exchange(value);
 }

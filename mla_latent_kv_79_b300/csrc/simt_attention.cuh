@@ -209,25 +209,27 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
     const int q = blockIdx.x;
     const int n_h = a.n_h, d_c = a.d_c;
     const int np = query_pages(a.qs, q);
-    // total pages and pages before q: one pass over seq_lens, two block sums
-    long long pq, total;
-    if (a.qs.mode == 1) {
-        pq = block_prefix_pages(a.qs, q, red);
-        total = block_prefix_pages(a.qs, a.qs.n_queries, red);
-    } else {
-        long long sq = 0, st = 0;
-        for (int i = threadIdx.x; i < a.qs.n_queries; i += blockDim.x) {
-            const int pi = query_pages(a.qs, i);
-            st += pi;
-            if (i < q) sq += pi;
+    // the partial slots of query q, as the attention kernel's schedule assigned them: partial i
+    // is in slot sbase + 2i, except that in the flat partition the first one is in slot
+    // 2*u_lo + 1 when the query starts after the beginning of unit u_lo (its second segment)
+    const Plan pl = block_plan(a.qs, a.n_units, red);
+    int ns = 0, sbase = 0, first_adj = 0;
+    if (pl.aligned) {
+        long long kb = 0;
+        for (int i = threadIdx.x; i < q; i += blockDim.x) kb += aligned_units(query_pages(a.qs, i), a.n_units, pl.total);
+        sbase = (int)(2 * block_sum_ll(kb, red));
+        if (np > 0) {
+            const long long k = aligned_units(np, a.n_units, pl.total), pc = (np + k - 1) / k;
+            ns = (int)((np + pc - 1) / pc);  // non-empty pieces
         }
-        pq = block_sum_ll(sq, red);
-        total = block_sum_ll(st, red);
+    } else {
+        const long long pq = block_prefix_pages(a.qs, q, red), per = pl.per;
+        const long long u_lo = pq / per;
+        if (np > 0) ns = (int)((pq + np - 1) / per - u_lo + 1);
+        sbase = (int)(2 * u_lo);
+        first_adj = pq == u_lo * per ? 0 : 1;
     }
-    long long per = (total + a.n_units - 1) / a.n_units;
-    if (per < 1) per = 1;
-    const long long u_lo = pq / per, u_hi = np > 0 ? (pq + np - 1) / per : u_lo;
-    if (np > 0 && u_lo == u_hi) return;  // written directly by the attention kernel
+    if (np > 0 && ns == 1) return;  // written directly by the attention kernel
 
     const int e = blockIdx.y * blockDim.x + threadIdx.x;
     if (e >= n_h * (d_c / V)) return;
@@ -240,8 +242,6 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
     }
     grid_dependency_wait();  // partials of the attention kernel are complete and visible
 
-    auto slot_of = [&](long long u) { return (u > u_lo || pq == u_lo * per) ? 2 * u : 2 * u + 1; };
-    const int ns = (int)(u_hi - u_lo + 1);
     float mx = -INFINITY, wsum = 0.f;
     float acc[V];
 #pragma unroll
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
             lv[j] = -INFINITY;
             v[j] = make_uint4(0u, 0u, 0u, 0u);
             if (i0 + j < ns) {
-                const long long sl = slot_of(u_lo + i0 + j);
+                const long long sl = sbase + 2 * (i0 + j) + (i0 + j == 0 ? first_adj : 0);
                 lv[j] = a.part_lse[sl * n_h + h];
                 v[j] = *reinterpret_cast<const uint4*>(po + part_index<T>(sl, h, V * grp, n_h, d_c));
             }

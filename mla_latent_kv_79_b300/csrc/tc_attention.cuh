@@ -24,9 +24,10 @@
 // is read while the line is still in L2.  The score-to-value traffic is one-directional, so
 // neither CTA waits on a round trip.
 //
-// The query of a segment travels through the score CTA's ring too: three items of three
-// 128-row x 64-column chunks, TMA-loaded and copied into TMEM by the MMA thread with
-// tcgen05.cp ahead of the segment's first QK (the tensor pipe keeps issue order).
+// The query of a segment travels through the score CTA's ring too: two items of nine 64-row x
+// 64-column boxes (144 KB, exactly two stages), so that the query and the segment's first page
+// are in flight together.  The softmax warps (idle at a segment start) move their rows into
+// TMEM with tcgen05.st, so the tensor pipe is not held up by the copy.
 //
 // Roles (192 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
 // (one TMEM lane quarter each, one head per thread) softmax in the score CTA, rescale and
@@ -47,8 +48,7 @@ constexpr int CHUNK = 64 * 128;                   // 64 rows x 64 bf16, 128-byte
 constexpr int LAT_CHUNKS = 8;
 constexpr int STAGES = 3;
 constexpr int S_STAGE_BYTES = 9 * CHUNK;          // score CTA: whole page, 9 chunks (72 KB)
-constexpr int Q_CHUNK = 128 * 128;                // 128 query rows x 64 bf16 (16 KB)
-constexpr int Q_ITEMS = 3;                        // ring items per query, three chunks each
+constexpr int Q_ITEMS = 2;                        // ring items per query, nine 8 KB boxes each
 constexpr int V_STAGE_BYTES = LAT_CHUNKS * CHUNK; // value CTA: latent part (64 KB)
 constexpr int OFF_R = STAGES * V_STAGE_BYTES;     // value CTA: P buffers
 constexpr int P_BYTES = NH * 128;                 // P [128 heads x 64 tokens] bf16, SW128 K-major
@@ -68,6 +68,7 @@ enum {
     B_PVDONE = B_PREADY + 2,     // [2] value CTA: PV of the page that used P buffer b complete
     B_OFREE = B_PVDONE + 2,      // value CTA: O drained
     B_DONE = B_OFREE + 1,        // MMA drain at exit
+    B_QREADY = B_DONE + 1,       // score CTA: the segment's query is in TMEM (4 softmax warps)
     NBARS
 };
 constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
@@ -147,13 +148,16 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
     const int nch = rank == 0 ? 9 : LAT_CHUNKS;
     const uint32_t stage_bytes = (uint32_t)(nch * CHUNK);
     while (ok && c.next(a.qs, &sg)) {
-        if (rank == 0) {  // the segment's query: three ring items of three 16 KB chunks
+        if (rank == 0) {  // the segment's query: box b of the 18 is (columns 64*(b/2), rows 64*(b%2))
             for (int qi = 0; qi < Q_ITEMS; ++qi, ++g) {
                 const uint32_t stage = g % STAGES;
                 if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
                 const uint32_t fb = bar_addr(base, B_FULL + stage), dst = base + stage * S_STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(fb, (uint32_t)(3 * Q_CHUNK));
-                for (int j = 0; j < 3; ++j) ptx::tma_load_2d(dst + j * Q_CHUNK, tmq, (3 * qi + j) * 64, sg.q * NH, fb);
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)S_STAGE_BYTES);
+                for (int j = 0; j < 9; ++j) {
+                    const int b = 9 * qi + j;
+                    ptx::tma_load_2d(dst + j * CHUNK, tmq, (b >> 1) * 64, sg.q * NH + (b & 1) * 64, fb);
+                }
             }
             if (!ok) break;
         }
@@ -183,28 +187,17 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
 // ----------------------------------------------------------------------------- score CTA
 __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
                                           const WaitCtl& wc) {
-    uint32_t g = 0, k = 0;  // pages, ring items
+    uint32_t g = 0, k = 0, segn = 0;  // pages, ring items, segments
     bool ok = true;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
-        // the segment's query into TMEM columns [TM_Q, TM_Q + 288).  A copy is ordered before
-        // the MMAs issued after it, but not after those issued before it: the previous
-        // segment's last QK (whose commit covers all earlier ones) must finish reading Q first.
-        if (g > 0 && !wait_bar(bar_addr(base, B_SFULL + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u, wc)) break;
-        for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) {
-            const uint32_t stage = k % STAGES;
-            if (!wait_bar(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint64_t dq = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    ptx::tmem_cp_128x256b(tmem + TM_Q + (3 * qi + j) * 32 + kk * 8,
-                                          dq + (uint64_t)((j * Q_CHUNK + kk * 32) >> 4));
-            ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
-        }
-        if (!ok) break;
+        // the softmax warps put the segment's query into TMEM columns [TM_Q, TM_Q + 288) (they
+        // do so only after reading the previous segment's last scores, i.e. after its QKs);
+        // then the three ring stages that carried it are free
+        if (!wait_bar(bar_addr(base, B_QREADY), segn & 1u, wc)) break;
+        ptx::tc_fence_after();
+        for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) ptx::mbar_arrive(bar_addr(base, B_EMPTY + k % STAGES));
+        ++segn;
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
             const uint32_t stage = k % STAGES, sb = g & 1u;
             if (!wait_bar(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
@@ -237,16 +230,44 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
     const int qd = warp & 3;  // TMEM lane quarter this warp may access
     const int h = qd * 32 + lane;
     const uint32_t lb = (uint32_t)(qd * 32) << 16;
-    const uint32_t tS = tmem + lb + TM_S;
+    const uint32_t tS = tmem + lb + TM_S, tQ = tmem + lb + TM_Q;
     const uint32_t pbuf_r = ptx::mapa(base + OFF_R, peer);          // value CTA's P buffers
     const uint32_t pfull_r = ptx::mapa(bar_addr(base, B_PFULL), peer);
     const uint32_t sw = (uint32_t)(h & 7);
-    uint32_t g = 0;
+    uint32_t g = 0, k = 0;  // pages, ring items
     bool ok = true;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
+        // this thread's query row (head h) from the two ring items into TMEM: 64-column chunk c
+        // of the row is 128 swizzled bytes (16-byte piece p at (p ^ (h & 7)) * 16) of box
+        // 2c + h/64, i.e. 32 columns of bf16 pairs
+        for (int qi = 0; qi < Q_ITEMS && ok; ++qi, ++k) {
+            const uint32_t stage = k % STAGES;
+            if (!warp_wait(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
+#pragma unroll
+            for (int j = 0; j < 9; ++j) {
+                const int b = 9 * qi + j;
+                if ((b & 1) != (h >> 6)) continue;  // warp-uniform: a quarter's heads share h / 64
+                const uint32_t row = base + stage * S_STAGE_BYTES + j * CHUNK + (uint32_t)(h & 63) * 128u;
+                uint32_t r[32];
+#pragma unroll
+                for (int pc = 0; pc < 8; ++pc) {
+                    const float4 v = ptx::ld_shared_v4(row + ((pc ^ sw) << 4));
+                    r[4 * pc + 0] = __float_as_uint(v.x);
+                    r[4 * pc + 1] = __float_as_uint(v.y);
+                    r[4 * pc + 2] = __float_as_uint(v.z);
+                    r[4 * pc + 3] = __float_as_uint(v.w);
+                }
+                ptx::tmem_st32(tQ + (b >> 1) * 32, r);
+            }
+        }
+        if (!ok) break;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_QREADY));
         float m_run = -INFINITY, l = 0.f;
-        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
             const uint32_t sb = g & 1u, use = g >> 1;
             if (!warp_wait(bar_addr(base, B_SFULL + sb), use & 1u, wc, false, lane)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -394,9 +415,9 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         }
         ptx::tc_fence_after();
         const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
-        // bf16 rows of O / l: the final output row, or the partial layout [slot][c/8][h][8]
-        // in which a warp's 32 heads write 512 contiguous bytes.  The TMEM load of the next
-        // 32 columns is in flight while the current ones are converted and stored.
+        // bf16 rows of O / l: the final output row o_lat[q][h][:], or the partial layout
+        // [slot][c/8][h][8] in which a warp's 32 heads write 512 contiguous bytes.  The TMEM
+        // load of the next 32 columns is in flight while the current ones are stored.
         uint4* dst;
         size_t step;
         if (sg.direct) {
@@ -454,9 +475,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // the split combine (a programmatic dependent) may be scheduled now; it waits for this
     // grid's completion before it reads anything this kernel writes
     launch_dependents();
-    // the schedule reads seq_lens first: start those lines towards L1 before the set-up below
-    if (a.qs.mode == 0 && threadIdx.x * 32 < a.qs.n_queries)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.qs.seq_lens + threadIdx.x * 32));
     const uint32_t rank = ptx::cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int unit = blockIdx.x >> 1;
@@ -477,6 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         ptx::mbar_init(bar_addr(base, B_OFREE), 4);
         ptx::mbar_init(bar_addr(base, B_DONE), 1);
+        ptx::mbar_init(bar_addr(base, B_QREADY), 4);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -493,6 +512,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     ptx::tc_fence_after();
     ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent, the set-up above overlaps the previous kernel;
+    // every input (queries, cache, page table, lengths) is read only after this wait.
+    grid_dependency_wait();
 
     UnitCursor cur;
     long long per;
@@ -561,11 +583,11 @@ inline bool tc_attention_supported(const mla_config* c, const mla_cache* k, int 
 }
 
 inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache, unsigned long long wait_ns,
-                                      cudaStream_t stream) {
+                                      bool pdl, cudaStream_t stream) {
     CUtensorMap tm, tmq;
     if (!tca::encode_pool_map(&tm, cache->pool, cache->num_pages)) return MLA_ERR_CUDA;
-    // the query rows viewed as [n_queries * 128, 576] bf16, box 64 columns x 128 rows
-    if (!tca::encode_pool_map(&tmq, const_cast<void*>(a.q_cat), (long long)a.qs.n_queries * tca::NH / tca::PAGE, 128))
+    // the query rows viewed as [n_queries * 128, 576] bf16, box 64 columns x 64 rows
+    if (!tca::encode_pool_map(&tmq, const_cast<void*>(a.q_cat), (long long)a.qs.n_queries * tca::NH / tca::PAGE))
         return MLA_ERR_CUDA;
     tca::TcArgs t;
     t.a = a;
@@ -574,8 +596,21 @@ inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache,
     if (cudaFuncSetAttribute(tca::tc_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tca::SMEM_BYTES) != cudaSuccess)
         return MLA_ERR_CUDA;
-    tca::tc_attention_kernel<<<2 * a.n_units, tca::NTHREADS, tca::SMEM_BYTES, stream>>>(tm, tmq, t);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * a.n_units);
+    lc.blockDim = dim3(tca::NTHREADS);
+    lc.dynamicSmemBytes = tca::SMEM_BYTES;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&lc, tca::tc_attention_kernel, tm, tmq, t) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    return MLA_OK;
 }
 
 inline bool tc_gemm_append_supported(const mla_config*, int) { return false; }
