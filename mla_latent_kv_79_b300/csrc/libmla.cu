@@ -300,9 +300,14 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
     const int W = d_c + d_r;
     DeviceInfo* dev;
     if ((st = device_info(&dev)) != MLA_OK) return st;
-    // RoPE half first: the GEMM that follows is its programmatic dependent, issues its weight
-    // loads at once and waits for the RoPE grid before loading q_nope, so the RoPE grid is
-    // complete whenever the GEMM is
+    const unsigned long long wait_ns = (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull;
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_absorb_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
+        // one tcgen05 kernel writes both halves of q_cat
+        st = tc_gemm_absorb(cfg, q_nope, q_rope, pos, w_uk, q_cat, n_tokens, gemm_tuning(wait_ns), s);
+        if (st != MLA_OK) return st;
+        count_launches(1);
+        return MLA_OK;
+    }
     const dim3 blocks(n_tokens, (n_h + ROPE_HEADS - 1) / ROPE_HEADS);
     RopeFreq rf;
     rope_freq_fill(&rf, d_r, cfg->rope_base);
@@ -312,23 +317,16 @@ mla_status mla_absorb_q(const mla_config* cfg, const void* q_nope, const void* q
         rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, rf);
     count_launches(1);
     if ((st = launch_status()) != MLA_OK) return st;
-    const unsigned long long wait_ns = (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull;
-    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_absorb_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
-        st = tc_gemm_absorb(cfg, q_nope, w_uk, q_cat, n_tokens, gemm_tuning(wait_ns), s);
-        if (st != MLA_OK) return st;
-        count_launches(1);
-    } else {
-        SimtGemmArgs g{};
-        g.A = q_nope; g.lda = (long long)n_h * d_h; g.a_batch = d_h;
-        g.B = w_uk; g.ldb_k = 1; g.ldb_n = (long long)n_h * d_h; g.b_batch = d_h;  // B(j,c) = W_UK[c, h*d_h+j]
-        g.C = q_cat; g.ldc = (long long)n_h * W; g.c_batch = W;
-        g.M = n_tokens; g.N = d_c; g.K = d_h;
-        dim3 grid((d_c + 63) / 64, (n_tokens + 63) / 64, n_h);
-        if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
-        else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
-        count_launches(1);
-        if ((st = launch_status()) != MLA_OK) return st;
-    }
+    SimtGemmArgs g{};
+    g.A = q_nope; g.lda = (long long)n_h * d_h; g.a_batch = d_h;
+    g.B = w_uk; g.ldb_k = 1; g.ldb_n = (long long)n_h * d_h; g.b_batch = d_h;  // B(j,c) = W_UK[c, h*d_h+j]
+    g.C = q_cat; g.ldc = (long long)n_h * W; g.c_batch = W;
+    g.M = n_tokens; g.N = d_c; g.K = d_h;
+    dim3 grid((d_c + 63) / 64, (n_tokens + 63) / 64, n_h);
+    if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    count_launches(1);
+    if ((st = launch_status()) != MLA_OK) return st;
     return MLA_OK;
 }
 

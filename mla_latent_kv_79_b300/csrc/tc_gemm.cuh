@@ -11,6 +11,9 @@
 // With few tokens (decode) a CTA's whole weight slice is in flight at once.  The kernel is
 // launched as a programmatic dependent: the weights do not depend on the previous kernel, so
 // their loads are issued before the grid-dependency wait and only the token operand after it.
+// In ABSORB mode the CTAs of the first m-tile also write the RoPE half of q_cat for their head
+// (RoPE(q_rope[n, h], pos[n]) into columns [d_c, d_c + d_r)), with the epilogue warps, which
+// are idle while the weights stream.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -63,6 +66,11 @@ struct GemmArgs {
     int hpc;            // heads per CTA
     void* out;          // q_cat (ABSORB) or o (OUT), bf16
     unsigned long long wait_ns;
+    // ABSORB: the RoPE half (q_rope [n, n_h, d_r] bf16 unrotated, pos [n]); q_rope may be null
+    const bf16* q_rope;
+    const int* pos;
+    int d_r;
+    RopeFreq rf;
 };
 
 // launch choices (0 = automatic), from the library's tuning knobs
@@ -195,6 +203,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;  // m within the tile
+        if (g.mode == ABSORB && mt == 0 && g.q_rope) {
+            grid_dependency_wait();  // q_rope and pos come from earlier kernels
+            const int half = g.d_r / 2, tid = threadIdx.x - 64;
+            const int n_here = min(g.n_pad, g.n_tokens - n0);
+            bf16* qc = reinterpret_cast<bf16*>(g.out);
+            for (int j = 0; j < nh; ++j) {
+                const int h = h0 + j;
+                for (int e = tid; e < n_here * half; e += NTHREADS - 64) {
+                    const int n = n0 + e / half, i = e % half;
+                    float c, sn;
+                    rope_cos_sin(__ldg(g.pos + n), g.rf.theta[i], &c, &sn);
+                    const __nv_bfloat162 x =
+                        *reinterpret_cast<const __nv_bfloat162*>(g.q_rope + ((size_t)n * g.n_h + h) * g.d_r + 2 * i);
+                    const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
+                    *reinterpret_cast<__nv_bfloat162*>(qc + ((size_t)n * g.n_h + h) * g.width + g.d_c + 2 * i) =
+                        __floats2bfloat162_rn(x0 * c - x1 * sn, x0 * sn + x1 * c);
+                }
+            }
+        }
         if (gwait(bar_done, 0, g.wait_ns)) {
             ptx::tc_fence_after();
             bf16* out = reinterpret_cast<bf16*>(g.out);
@@ -295,12 +322,16 @@ inline bool tc_gemm_out_supported(const mla_config* c, int n, int cc_major, int 
            c->d_latent % 64 == 0;
 }
 
-// q_cat[:, :, 0:d_c] of mla_absorb_q (the RoPE half is written by rope_query_kernel)
-inline mla_status tc_gemm_absorb(const mla_config* c, const void* q_nope, const void* w_uk, void* q_cat, int n,
-                                 const tcg::Tuning& t, cudaStream_t stream) {
+// the whole of q_cat for mla_absorb_q: the GEMM half and, in the first m-tile's CTAs, RoPE
+inline mla_status tc_gemm_absorb(const mla_config* c, const void* q_nope, const void* q_rope, const int* pos,
+                                 const void* w_uk, void* q_cat, int n, const tcg::Tuning& t, cudaStream_t stream) {
     tcg::GemmArgs g{};
     g.mode = tcg::ABSORB;
     g.n_tokens = n;
+    g.q_rope = reinterpret_cast<const bf16*>(q_rope);
+    g.pos = pos;
+    g.d_r = c->d_rope;
+    rope_freq_fill(&g.rf, c->d_rope, c->rope_base);
     g.n_pad = tcg::n_pad_for(n);
     g.k_chunks = c->d_nope / tcg::BK;
     g.n_h = c->n_heads; g.d_h = c->d_nope; g.d_c = c->d_latent; g.width = c->d_latent + c->d_rope;
