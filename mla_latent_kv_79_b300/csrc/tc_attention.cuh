@@ -273,15 +273,16 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             ptx::tc_fence_after();
             float s[64];
             {
-                uint32_t r[32];
-                ptx::tmem_ld32(tS + sb * 64, r);
-                ptx::tmem_wait_ld();
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld32(tS + sb * 64, r0);
+                ptx::tmem_ld32(tS + sb * 64 + 32, r1);
+                ptx::tmem_wait_ld_regs(r0);
+                ptx::tmem_wait_ld_regs(r1);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
-                ptx::tmem_ld32(tS + sb * 64 + 32, r);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = __uint_as_float(r0[j]);
+                    s[32 + j] = __uint_as_float(r1[j]);
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -416,8 +417,9 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         ptx::tc_fence_after();
         const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
         // bf16 rows of O / l: the final output row o_lat[q][h][:], or the partial layout
-        // [slot][c/8][h][8] in which a warp's 32 heads write 512 contiguous bytes.  The TMEM
-        // load of the next 32 columns is in flight while the current ones are stored.
+        // [slot][c/8][h][8] in which a warp's 32 heads write 512 contiguous bytes.  Four TMEM
+        // loads (128 columns) are in flight per wait: the load latency, not the stores, set the
+        // pace when each 32-column load was waited for on its own.
         uint4* dst;
         size_t step;
         if (sg.direct) {
@@ -438,19 +440,21 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
                 dst[(size_t)(4 * k + i) * step] = v;
             }
         };
-        {
-            uint32_t ra[32], rb[32];
-            ptx::tmem_ld32(tO, ra);
-            ptx::tmem_wait_ld_regs(ra);
-#pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-                ptx::tmem_ld32(tO + 32 * (k + 1), rb);
-                emit(ra, k);
-                ptx::tmem_wait_ld_regs(rb);
-                if (k + 2 < 16) ptx::tmem_ld32(tO + 32 * (k + 2), ra);
-                emit(rb, k + 1);
-                if (k + 2 < 16) ptx::tmem_wait_ld_regs(ra);
-            }
+#pragma unroll 1
+        for (int k0 = 0; k0 < 16; k0 += 4) {
+            uint32_t r0[32], r1[32], r2[32], r3[32];
+            ptx::tmem_ld32(tO + 32 * k0, r0);
+            ptx::tmem_ld32(tO + 32 * (k0 + 1), r1);
+            ptx::tmem_ld32(tO + 32 * (k0 + 2), r2);
+            ptx::tmem_ld32(tO + 32 * (k0 + 3), r3);
+            ptx::tmem_wait_ld_regs(r0);
+            ptx::tmem_wait_ld_regs(r1);
+            ptx::tmem_wait_ld_regs(r2);
+            ptx::tmem_wait_ld_regs(r3);
+            emit(r0, k0);
+            emit(r1, k0 + 1);
+            emit(r2, k0 + 2);
+            emit(r3, k0 + 3);
         }
         ptx::tc_fence_before();
         __syncwarp();
