@@ -32,6 +32,14 @@
  *   - Slots of the pool that no token owns must hold finite values (masked tokens still
  *     meet a zero weight: 0 * finite = 0).
  *   - lse is the natural-log log-sum-exp of the scaled scores of one (query, head).
+ *   - Kernels are launched with programmatic dependent launch: a kernel of this library may
+ *     start while the kernel before it in the stream finishes, if that kernel allows it
+ *     (griddepcontrol.launch_dependents; the library's own kernels do).  It waits for that
+ *     kernel before reading what that kernel may write: q_cat in mla_decode / mla_prefill
+ *     (written by mla_absorb_q), o_lat in mla_out, q_nope / q_rope / pos in mla_absorb_q.
+ *     The cache, page table and lengths are read without that wait, so they must be produced
+ *     by work that completes before the preceding kernel starts (ordinary kernels and copies
+ *     do; MLA_TUNE_NO_PDL turns programmatic launch off).
  *
  * Error behaviour: a non-OK status means nothing was launched, except MLA_ERR_CUDA, which
  * reports the CUDA error of a launch (cudaGetLastError is cleared).

@@ -147,7 +147,27 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
     Segment sg;
     const int nch = rank == 0 ? 9 : LAT_CHUNKS;
     const uint32_t stage_bytes = (uint32_t)(nch * CHUNK);
+    bool waited = false;
     while (ok && c.next(a.qs, &sg)) {
+        int pg0 = sg.page_begin;
+        bool early = false;  // this segment's first page went out before the query
+        if (rank == 0 && !waited) {
+            // The query is the one input written by the kernel just before (the absorption
+            // GEMM, whose dependants may start early): the unit's first page (ring item 2, a
+            // free stage) goes out before the grid-dependency wait, the query after it.
+            int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + pg0);
+            if (page < 0 || page >= a.num_pages) {
+                set_device_error(MLA_ERR_DEVICE_BOUNDS);
+                page = 0;
+            }
+            const uint32_t stage = (g + Q_ITEMS) % STAGES, fb = bar_addr(base, B_FULL + stage);
+            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+            for (int cc = 0; cc < nch; ++cc)
+                ptx::tma_load_2d(base + stage * stage_bytes + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
+            grid_dependency_wait();
+            waited = true;
+            early = true;
+        }
         if (rank == 0) {  // the segment's query: box b of the 18 is (columns 64*(b/2), rows 64*(b%2))
             for (int qi = 0; qi < Q_ITEMS; ++qi, ++g) {
                 const uint32_t stage = g % STAGES;
@@ -160,8 +180,12 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                 }
             }
             if (!ok) break;
+            if (early) {  // ring item g (the first page) is already in flight
+                ++pg0;
+                ++g;
+            }
         }
-        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+        for (int pg = pg0; pg < sg.page_end; ++pg, ++g) {
             const uint32_t stage = g % STAGES;
             if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
             int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + pg);
@@ -203,16 +227,18 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
             if (!wait_bar(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
             if (!wait_bar(bar_addr(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
             ptx::tc_fence_after();
-            // fully unrolled issue: descriptors are the stage's base descriptor plus constant
-            // offsets (the 14-bit address field cannot carry: shared addresses are < 256 KB)
+            // descriptors are the stage's base descriptor plus offsets (the 14-bit address field
+            // cannot carry: shared addresses are < 256 KB); one 64-column chunk per iteration
+            // keeps the code short (it is fetched cold after every L2 flush)
             const uint64_t d_pg = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
             const uint32_t d = tmem + TM_S + sb * 64;
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 9; ++cc) {
+                const uint64_t dc = d_pg + (uint64_t)((cc * CHUNK) >> 4);
+                const uint32_t ac = tmem + TM_Q + cc * 32;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA, 4 per 64-column chunk
-                    ptx::mma_ts(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
-                                IDESC_QK, (cc | kk) ? 1u : 0u);
+                    ptx::mma_ts(d, ac + kk * 8, dc + (uint64_t)((kk * 32) >> 4), IDESC_QK, (cc | kk) ? 1u : 0u);
             }
             ptx::tc_commit(bar_addr(base, B_SFULL + sb));
             ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
@@ -244,7 +270,7 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
         for (int qi = 0; qi < Q_ITEMS && ok; ++qi, ++k) {
             const uint32_t stage = k % STAGES;
             if (!warp_wait(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < 9; ++j) {
                 const int b = 9 * qi + j;
                 if ((b & 1) != (h >> 6)) continue;  // warp-uniform: a quarter's heads share h / 64
@@ -516,9 +542,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     ptx::tc_fence_after();
     ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
-    // Launched as a programmatic dependent, the set-up above overlaps the previous kernel;
-    // every input (queries, cache, page table, lengths) is read only after this wait.
-    grid_dependency_wait();
+    // Launched as a programmatic dependent, this kernel may start while the one before it (the
+    // absorption GEMM) finishes.  Only the queries come from that kernel: the score CTA's
+    // producer waits for it (griddepcontrol.wait) before their loads; lengths, page table and
+    // cache come from earlier work and are read at once.
 
     UnitCursor cur;
     long long per;

@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (threadIdx.x == 0) set_device_error(MLA_ERR_UNSUPPORTED);
         return;
     }
+    // the next kernel (the attention, or this GEMM's successor) may be placed as SMs free up;
+    // it waits for this grid before it reads what this grid writes
+    launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x, h0 = blockIdx.y * g.hpc, n0 = blockIdx.z * MAX_N;
     const int nh = min(g.hpc, g.n_h - h0);
