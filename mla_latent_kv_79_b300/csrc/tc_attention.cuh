@@ -344,8 +344,8 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             const uint32_t row = pbuf_r + pb * PBUF_BYTES + (uint32_t)h * 128u;
             const uint32_t fb = pfull_r + 8u * pb;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                ptx::st_async_v4_b32(row + ((k ^ sw) << 4), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3], fb);
+            for (int c = 0; c < 8; ++c)
+                ptx::st_async_v4_b32(row + ((c ^ sw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3], fb);
             ptx::st_async_v2_f32(pbuf_r + pb * PBUF_BYTES + P_BYTES + (uint32_t)h * 8u, alpha, l, fb);
         }
         if (!ok) break;
@@ -419,13 +419,20 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
                 }
                 ptx::tc_fence_after();
                 const float alpha = resc ? meta.x : 1.f;
-                for (int k = 0; k < 16; ++k) {
-                    uint32_t r[32];
-                    ptx::tmem_ld32(tO + 32 * k, r);
-                    ptx::tmem_wait_ld();
+#pragma unroll 1
+                for (int k0 = 0; k0 < 16; k0 += 2) {  // two loads in flight per wait
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld32(tO + 32 * k0, r0);
+                    ptx::tmem_ld32(tO + 32 * (k0 + 1), r1);
+                    ptx::tmem_wait_ld_regs(r0);
+                    ptx::tmem_wait_ld_regs(r1);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                    ptx::tmem_st32(tO + 32 * k, r);
+                    for (int j = 0; j < 32; ++j) {
+                        r0[j] = __float_as_uint(__uint_as_float(r0[j]) * alpha);
+                        r1[j] = __float_as_uint(__uint_as_float(r1[j]) * alpha);
+                    }
+                    ptx::tmem_st32(tO + 32 * k0, r0);
+                    ptx::tmem_st32(tO + 32 * (k0 + 1), r1);
                 }
                 ptx::tmem_wait_st();
             }

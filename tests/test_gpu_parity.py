@@ -237,6 +237,32 @@ def test_decode_split_then_multipage_segment(path, lens, units):
     assert_no_device_error()
 
 
+@pytest.mark.parametrize("units", [1, 3])
+def test_decode_running_max_jumps(path, units):
+    """Later cache rows scaled by 4 and then 16 (exact in bf16): the scores jump by far more
+    than the lazy-rescale threshold, so O and l are rescaled mid-segment."""
+    lens = [1000, 2049]
+    case = W.make_decode_case(DS, "bf16", lens, seed=59)
+    pool = case["pool"].copy()
+    for b, L in enumerate(lens):
+        rows = W.bf16_bits_to_f32(W.gather_rows(pool, case["page_table"][b], L)).copy()
+        rows[128:] *= 4.0
+        rows[640:] *= 4.0
+        W.scatter_rows(pool, case["page_table"][b], W.quantise(rows, "bf16"))
+    case = dict(case, pool=pool)
+    old = M.mla_set_tuning(_lib.MLA_TUNE_ATTN_UNITS, units)
+    try:
+        o, l = M.mla_decode(cfg_of(DS, "bf16"), cache_of(case), dev(case["q_cat"]))
+    finally:
+        M.mla_set_tuning(_lib.MLA_TUNE_ATTN_UNITS, old)
+    go, gl = host(o), host(l)
+    for b in range(len(lens)):
+        ro, rl = oracle_decode(case, b)
+        assert rel(go[b], ro) <= TOL_OUT_BF16, b
+        assert np.max(np.abs(gl[b] - rl)) <= TOL_LSE_BF16, b
+    assert_no_device_error()
+
+
 def test_decode_page_table_is_bit_exact(path):
     """A shuffled page table gives bit-identical results to the identity table over the
     same token data (paging is pure indexing)."""
