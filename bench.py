@@ -46,13 +46,19 @@ def peaks():
 
 
 def workload_numbers(case):
-    """Algorithmic bytes and FLOPs of one decode launch (the split-attention kernel):
-    cache rows read once (L*W*2), queries (n_h*W*2), outputs (n_h*(d_c*2+4)) per sequence;
-    FLOPs 2*L*n_h*(W + d_c) per sequence (scores plus weighted sum)."""
+    """Algorithmic bytes and FLOPs of one attention launch (the split-attention kernel).
+    Decode: cache rows read once (L*W*2), queries (n_h*W*2), outputs (n_h*(d_c*2+4)) per
+    sequence; FLOPs 2*L*n_h*(W + d_c) per sequence (scores plus weighted sum).
+    Causal prefill of T queries: the T cache rows once, T queries and outputs; query i
+    attends i+1 tokens, so FLOPs 2*n_h*(W + d_c)*T(T+1)/2."""
     s = case["shape"]
-    L = case["seq_lens"].astype(np.int64)
     Wd = s.width
-    bytes_ = int(np.sum(L * Wd * 2 + s.n_heads * Wd * 2 + s.n_heads * (s.d_latent * 2 + 4)))
+    per_q = s.n_heads * Wd * 2 + s.n_heads * (s.d_latent * 2 + 4)
+    if "T" in case:
+        T = int(case["T"])
+        return T * Wd * 2 + T * per_q, s.n_heads * (Wd + s.d_latent) * T * (T + 1)
+    L = case["seq_lens"].astype(np.int64)
+    bytes_ = int(np.sum(L * Wd * 2 + per_q))
     flops = int(np.sum(2 * L * s.n_heads * (Wd + s.d_latent)))
     return bytes_, flops
 
@@ -178,6 +184,10 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    if W.WORKLOADS[args.workload].mode not in ("decode", "append_decode"):
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the decode workloads only"}),
+              flush=True)
+        return 0
     case = W.make_workload(args.workload)
     for _ in range(max(0, args.warmup)):
         cpu_oracle_sample(case, 1)
@@ -200,7 +210,13 @@ def run_reference(args):
 
 def config_of(name, case):
     s = case["shape"]
-    return {"workload": name, "batch": int(case["seq_lens"].shape[0]),
+    w = W.WORKLOADS[name]
+    extra = {"step": {"decode": "absorb_q + decode + out",
+                      "append_decode": "cache_append (one token per sequence) + absorb_q + decode + out",
+                      "prefill": "cache_append (T tokens) + absorb_q + causal prefill + out"}[w.mode]}
+    if "T" in case:
+        extra["query_tokens"] = int(case["T"])
+    return {"workload": name, "batch": int(case["seq_lens"].shape[0]), **extra,
             "seq_len": int(case["seq_lens"].max()), "n_heads": s.n_heads, "d_nope": s.d_nope,
             "d_rope": s.d_rope, "d_latent": s.d_latent, "page_size": s.page_size,
             "page_table": "shuffled", "l2": "flushed between steps (256 MB write)"}
@@ -229,16 +245,24 @@ def run_ours(args):
     import mla_latent_kv_79_b300 as M
 
     case = W.make_workload(args.workload)
+    mode = W.WORKLOADS[args.workload].mode
+    if mode == "tiny_decode":
+        raise SystemExit("the tiny fp32 workload is a parity case, not a benchmark")
     s = case["shape"]
     cfg = M.MLAConfig.from_shape(s, case["dtype"])
     dt = case["dtype"]
     dev = lambda a: W.to_device(a, dt)  # noqa: E731
-    cache = M.PagedCache(dev(case["pool"]), torch.from_numpy(case["page_table"]).cuda(),
-                         torch.from_numpy(case["seq_lens"]).cuda())
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()  # noqa: E731
+    cache = M.PagedCache(dev(case["pool"]), i32(case["page_table"]), i32(case["seq_lens"]))
     q_nope, q_rope = dev(case["q_nope"]), dev(case["q_rope"])
-    pos = torch.from_numpy(case["pos"]).cuda()
+    prefill = mode == "prefill"
+    pos = i32(case["append_pos"] if prefill else case["pos"])
     w_uk, w_uv = dev(case["w_uk"]), dev(case["w_uv"])
-    B = int(case["seq_lens"].shape[0])
+    appending = mode in ("append_decode", "prefill")
+    if appending:
+        x, w_dkv, w_kr = dev(case["x"]), dev(case["w_dkv"]), dev(case["w_kr"])
+        a_seq, a_pos = i32(case["append_seq"]), i32(case["append_pos"])
+    B = int(case["T"]) if prefill else int(case["seq_lens"].shape[0])  # query tokens per step
     q_cat = torch.empty((B, s.n_heads, s.width), dtype=cfg.torch_dtype, device="cuda")
     o_lat = torch.empty((B, s.n_heads, s.d_latent), dtype=cfg.torch_dtype, device="cuda")
     lse = torch.empty((B, s.n_heads), dtype=torch.float32, device="cuda")
@@ -248,8 +272,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def step():
+        if appending:  # the same positions every step: the cache ends each step identical
+            M.mla_cache_append(cfg, cache, x, w_dkv, w_kr, a_seq, a_pos, stream=stream)
         M.mla_absorb_q(cfg, q_nope, q_rope, pos, w_uk, q_cat=q_cat, stream=stream)
-        M.mla_decode(cfg, cache, q_cat, o_lat=o_lat, lse=lse, workspace=ws, stream=stream)
+        if prefill:
+            M.mla_prefill(cfg, cache, 0, 0, q_cat, o_lat=o_lat, lse=lse, workspace=ws, stream=stream)
+        else:
+            M.mla_decode(cfg, cache, q_cat, o_lat=o_lat, lse=lse, workspace=ws, stream=stream)
         M.mla_out(cfg, o_lat, w_uv, o=o, stream=stream)
 
     warm = max(3, args.warmup)
@@ -301,6 +330,7 @@ def run_ours(args):
     # host memory and read the output back
     h_qn = q_nope.cpu().pin_memory()
     h_qr = q_rope.cpu().pin_memory()
+    h_x = x.cpu().pin_memory() if appending else None
     h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -312,6 +342,8 @@ def run_ours(args):
         eev[i][0].record(stream)
         q_nope.copy_(h_qn, non_blocking=True)
         q_rope.copy_(h_qr, non_blocking=True)
+        if appending:
+            x.copy_(h_x, non_blocking=True)
         step()
         h_o.copy_(o, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
@@ -330,6 +362,7 @@ def run_ours(args):
     hbm, tflops, src = peaks()
     k_mean_s = (sum(kern_ms) / K) * 1e-3
     achieved = alg_bytes / k_mean_s / 1e9
+    tensor_bound = alg_flops / (tflops * 1e12) > alg_bytes / (hbm * 1e9)
     kernel_key = "tc_attention" if path == 2 else "simt_attention"
     line = {
         "metric": METRIC,
@@ -345,21 +378,26 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": config_of(args.workload, case),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": ncu_traffic(kernel_key, args.workload),
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm",
+                     "achieved": alg_flops / k_mean_s / 1e12 if tensor_bound else achieved,
+                     "peak": tflops if tensor_bound else hbm, "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                     "frac": (alg_flops / k_mean_s / 1e12 / tflops) if tensor_bound else achieved / hbm,
+                     "traffic": ncu_traffic(kernel_key, args.workload), "gbs": achieved,
                      "kernel": kernel_key, "kernel_us": k_mean_s * 1e6,
                      "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
                      "tflops": alg_flops / k_mean_s / 1e12, "peak_source": src,
                      "tensor_frac": alg_flops / k_mean_s / 1e12 / tflops,
                      "roofline_us": 1e6 * max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12))},
         "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size()),
+                "h2d_bytes_per_step": int(h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size()
+                                          + (h_x.numel() * h_x.element_size() if appending else 0)),
                 "d2h_bytes_per_step": int(h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size())},
         "gpu_launches": int(launches),
         "clocks": clock,
+        "cpu_baseline": None,
         "step_us_median": 1e3 * statistics.median(step_ms),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not appending:
         n_seq = 0
         t_cpu = 0.0
         while n_seq < B and t_cpu < 10.0:

@@ -266,8 +266,15 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const
     if (!aligned16(x) || !aligned16(w_dkv) || !aligned16(w_kr)) return MLA_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int W = cfg->d_latent + cfg->d_rope;
-    if (tc_gemm_append_supported(cfg, n_tokens) && !g_tune[MLA_TUNE_FORCE_SIMT].load())
-        return tc_gemm_append(cfg, cache, x, w_dkv, w_kr, seq_idx, pos, n_tokens, s);
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_append_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor) &&
+        (long long)cache->num_pages * cfg->page_size < (1LL << 31)) {
+        st = tc_gemm_append(cfg, cache, x, w_dkv, w_kr, seq_idx, pos, n_tokens,
+                            gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull), s);
+        if (st == MLA_OK) count_launches(1);
+        return st;
+    }
     SimtGemmArgs g{};
     g.A = x; g.lda = cfg->d_model; g.a_batch = 0;
     g.B = w_dkv; g.ldb_k = cfg->d_latent; g.ldb_n = 1; g.b_batch = 0;

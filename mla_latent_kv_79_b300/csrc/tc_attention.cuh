@@ -651,10 +651,4 @@ inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache,
     return MLA_OK;
 }
 
-inline bool tc_gemm_append_supported(const mla_config*, int) { return false; }
-inline mla_status tc_gemm_append(const mla_config*, const mla_cache*, const void*, const void*, const void*,
-                                 const int32_t*, const int32_t*, int32_t, cudaStream_t) {
-    return MLA_ERR_UNSUPPORTED;
-}
-
 }  // namespace mla

@@ -2,10 +2,12 @@
 //
 //   absorb: q_cat[n, h, c] = sum_j W_UK[c, h*d_h + j] * q_nope[n, h, j]      (M = c, K = j)
 //   out:    o[n, h*d_h + j] = sum_c W_UV[c, h*d_h + j] * o_lat[n, h, c]       (M = j, K = c)
+//   append: row[n, c] = sum_k [W_DKV | W_KR][k, c] * x[n, k], stored to the paged pool with
+//           RoPE(., pos[n]) on the last d_r columns                            (M = c, K = k)
 //
-// Both are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
-// 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, as the weight is stored) and
-// up to 256 tokens as B (K-major).  Each CTA owns one m-tile of up to HPC heads for one n-tile:
+// All are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
+// 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, W_DKV and W_KR, as the
+// weights are stored) and up to 256 tokens as B (K-major).  Each CTA owns one m-tile of up to HPC heads for one n-tile:
 // warp 0 streams 64-wide K chunks of A and B through a ring that fills shared memory, warp 1
 // issues the MMAs into one TMEM accumulator per head, warps 2-5 drain D (one row per thread).
 // With few tokens (decode) a CTA's whole weight slice is in flight at once.  The kernel is
@@ -30,7 +32,8 @@ constexpr int SMEM_LIMIT = 232448;            // opt-in shared memory per CTA
 
 // stage = A tile + B tile (n_pad rows of 128 B), rounded to the 1 KB swizzle atom
 __host__ __device__ inline int stage_bytes(int n_pad) { return (A_BYTES + n_pad * BK * 2 + 1023) & ~1023; }
-__host__ __device__ inline int smem_bytes(int n_pad, int stages) { return stages * stage_bytes(n_pad) + 16 * stages + 32; }
+// ring, barriers, TMEM slot, then (APPEND) the pool row offset of each token of the tile
+__host__ __device__ inline int smem_bytes(int n_pad, int stages) { return stages * stage_bytes(n_pad) + 16 * stages + 48 + 4 * MAX_N; }
 __host__ __device__ inline uint32_t tmem_cols(int n_pad) {
     uint32_t c = 32;
     while ((int)c < n_pad) c <<= 1;
@@ -40,7 +43,7 @@ __host__ __device__ inline uint32_t tmem_cols(int n_pad) {
 // weight streams gain from more resident CTAs, not from a deeper ring per CTA).  Many tokens:
 // as deep as shared memory allows.
 inline int max_stages(int n_pad) {
-    int s = (SMEM_LIMIT - 32) / (stage_bytes(n_pad) + 16);
+    int s = (SMEM_LIMIT - 48 - 4 * MAX_N) / (stage_bytes(n_pad) + 16);
     return s < MAX_STAGES ? s : MAX_STAGES;
 }
 inline int stages_for(int n_pad) {
@@ -54,7 +57,7 @@ inline int max_heads_per_cta(int n_pad) {
     return h < HPC ? h : HPC;
 }
 
-enum Mode { ABSORB = 0, OUT = 1 };
+enum Mode { ABSORB = 0, OUT = 1, APPEND = 2 };
 
 struct GemmArgs {
     int mode;
@@ -71,6 +74,13 @@ struct GemmArgs {
     const int* pos;
     int d_r;
     RopeFreq rf;
+    int n_tile;         // tokens per CTA tile (the grid's z dimension walks them)
+    // APPEND: the paged pool and where each token goes (pos is the token's position)
+    void* pool;
+    const int* page_table;
+    const int* seq_idx;
+    int max_pages, batch, page_size;
+    long long num_pages;
 };
 
 // launch choices (0 = automatic), from the library's tuning knobs
@@ -105,9 +115,27 @@ __device__ __forceinline__ int chunk_k(const GemmArgs& g, int c, int nh) {
     return g.mode == OUT ? c / nh : c % g.k_chunks;
 }
 
-// grid: (m-tiles, ceil(n_h / hpc), n-tiles)
+// Pool row (element offset) of appended token n, or -1 (and the bounds error) when its sequence,
+// position or page is outside the cache.
+__device__ __forceinline__ long long append_row(const GemmArgs& g, int n) {
+    const int b = __ldg(g.seq_idx + n), p = __ldg(g.pos + n);
+    if (b < 0 || b >= g.batch || p < 0 || p >= g.max_pages * g.page_size) {
+        set_device_error(MLA_ERR_DEVICE_BOUNDS);
+        return -1;
+    }
+    const int page = __ldg(g.page_table + (long long)b * g.max_pages + p / g.page_size);
+    if (page < 0 || page >= g.num_pages) {
+        set_device_error(MLA_ERR_DEVICE_BOUNDS);
+        return -1;
+    }
+    return ((long long)page * g.page_size + p % g.page_size) * g.width;
+}
+
+// grid: (m-tiles, ceil(n_h / hpc), n-tiles).  tmA2 is W_KR in APPEND mode (its m-tile is the
+// last one), otherwise unused.
 __global__ void __launch_bounds__(NTHREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA2, const GemmArgs g) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base = ptx::smem_u32(smem);
     if (base & 1023u) {
@@ -118,14 +146,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // it waits for this grid before it reads what this grid writes
     launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, h0 = blockIdx.y * g.hpc, n0 = blockIdx.z * MAX_N;
+    const int mt = blockIdx.x, h0 = blockIdx.y * g.hpc, n0 = blockIdx.z * g.n_tile;
     const int nh = min(g.hpc, g.n_h - h0);
     const int S = g.stages, SB = stage_bytes(g.n_pad);
     const uint32_t acc_cols = tmem_cols(g.n_pad);                  // columns per head accumulator
     const uint32_t ncols = tmem_cols((int)acc_cols * g.hpc);
     const uint32_t bar_full = base + S * SB, bar_empty = bar_full + 8 * S, bar_done = bar_empty + 8 * S;
     const uint32_t slot = bar_done + 8;
-    const bool a_mn = g.mode == OUT;
+    int* rowoff = reinterpret_cast<int*>(smem + (bar_done - base) + 16);  // APPEND: [n_pad] (in units of W)
+    const bool a_mn = g.mode != ABSORB;
+    const bool rope_tile = g.mode == APPEND && mt * BM >= g.d_c;
     const int total = nh * g.k_chunks;                             // chunks of this CTA, head-major
 
     if (threadIdx.x == 0) {
@@ -137,7 +167,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(rope_tile ? &tmA2 : &tmA);
         ptx::prefetch_tmap(&tmB);
     }
     if (warp == 1) {
@@ -156,6 +186,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (g.mode == ABSORB) {
                 // W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + kc * BK, mt * BM, fb);
+            } else if (g.mode == APPEND) {
+                // W_DKV (or, for the last tile, W_KR) rows k in [kc*64, +64) x output columns
+                // m .. m + 128 (MN-major, two boxes; columns past d_r read as zeros)
+                const CUtensorMap* t = rope_tile ? &tmA2 : &tmA;
+                const int m0 = rope_tile ? 0 : mt * BM;
+                ptx::tma_load_2d(st, t, m0, kc * BK, fb);
+                ptx::tma_load_2d(st + BK * 128, t, m0 + 64, kc * BK, fb);
             } else {
                 // W_UV rows c in [kc*64, +64) x cols h*d_h + mt*128 + {0, 64} (MN-major, two boxes)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + mt * BM, kc * BK, fb);
@@ -164,8 +201,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         };
         auto load_b = [&](int c, uint32_t st, uint32_t fb) {
             const int h = h0 + chunk_head(g, c, nh), kc = chunk_k(g, c, nh);
-            // q_nope viewed [n, n_h*d_h] (ABSORB) or o_lat viewed [n, n_h*d_c] (OUT)
-            const int col = (g.mode == ABSORB ? h * g.d_h : h * g.d_c) + kc * BK;
+            // q_nope viewed [n, n_h*d_h] (ABSORB), o_lat viewed [n, n_h*d_c] (OUT) or x [n, d_model]
+            const int col = (g.mode == ABSORB ? h * g.d_h : g.mode == OUT ? h * g.d_c : 0) + kc * BK;
             ptx::tma_load_2d(st + A_BYTES, &tmB, col, n0, fb);
         };
         // the first ring's worth of weights goes out before the previous kernel has finished
@@ -225,7 +262,72 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        if (gwait(bar_done, 0, g.wait_ns)) {
+        const int tid = threadIdx.x - 64, n_here = min(g.n_pad, g.n_tokens - n0);
+        if (g.mode == APPEND) {
+            // where each token of the tile goes (inputs of earlier kernels: after the wait)
+            grid_dependency_wait();
+            for (int i = tid; i < n_here; i += NTHREADS - 64) {
+                const long long r = append_row(g, n0 + i);
+                rowoff[i] = r < 0 ? -1 : (int)(r / g.width);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        // the four epilogue warps agree on the outcome of the wait (they meet at named barriers)
+        bool done_ok = false;
+        if (g.mode == APPEND) {
+            const bool mine = gwait(bar_done, 0, g.wait_ns);
+            uint32_t all;
+            asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
+                         "selp.u32 %0, 1, 0, q;\n\t}"
+                         : "=r"(all)
+                         : "r"((uint32_t)mine)
+                         : "memory");
+            done_ok = all != 0;
+        }
+        if (g.mode == APPEND && done_ok) {
+            ptx::tc_fence_after();
+            bf16* pool = reinterpret_cast<bf16*>(g.pool);
+            const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
+            if (!rope_tile) {
+                // latent columns: per token, the 128 threads write 128 consecutive values
+                const int c = mt * BM + row;
+                for (int c0 = 0; c0 < g.n_pad; c0 += 32) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(taddr + c0, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if (c0 + i < n_here && rowoff[c0 + i] >= 0)
+                            pool[(size_t)rowoff[c0 + i] * g.width + c] = __float2bfloat16_rn(__uint_as_float(r[i]));
+                    }
+                }
+            } else {
+                // RoPE columns: the pair (2i, 2i+1) sits in two threads, so the fp32 values go
+                // through shared memory (the ring is idle now: every MMA has completed)
+                float* stg = reinterpret_cast<float*>(smem);  // [n_pad][d_r]
+                for (int c0 = 0; c0 < g.n_pad; c0 += 32) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(taddr + c0, r);
+                    ptx::tmem_wait_ld();
+                    if (row < g.d_r) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c0 + i < g.n_pad) stg[(c0 + i) * g.d_r + row] = __uint_as_float(r[i]);
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                const int half = g.d_r / 2;
+                for (int e = tid; e < n_here * half; e += NTHREADS - 64) {
+                    const int nl = e / half, i = e % half;
+                    if (rowoff[nl] < 0) continue;
+                    float cs, sn;
+                    rope_cos_sin(__ldg(g.pos + n0 + nl), g.rf.theta[i], &cs, &sn);
+                    const float x0 = stg[nl * g.d_r + 2 * i], x1 = stg[nl * g.d_r + 2 * i + 1];
+                    *reinterpret_cast<__nv_bfloat162*>(pool + (size_t)rowoff[nl] * g.width + g.d_c + 2 * i) =
+                        __floats2bfloat162_rn(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+                }
+            }
+        } else if (g.mode != APPEND && gwait(bar_done, 0, g.wait_ns)) {
             ptx::tc_fence_after();
             bf16* out = reinterpret_cast<bf16*>(g.out);
             for (int j = 0; j < nh; ++j) {
@@ -286,11 +388,13 @@ inline int n_pad_for(int n) {
     return (p + 15) & ~15;
 }
 
-inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtensorMap& b, int m_tiles, int n_h,
-                         const Tuning& t, cudaStream_t stream) {
+inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a2,
+                         int m_tiles, int n_h, const Tuning& t, cudaStream_t stream) {
     GemmArgs g = g0;
     g.wait_ns = t.wait_ns;
-    g.stages = stages_for(g.n_pad);
+    if (g.n_tile == 0) g.n_tile = MAX_N;
+    // APPEND streams K = d_model in 64-wide chunks per CTA: as deep a ring as fits
+    g.stages = g.mode == APPEND ? max_stages(g.n_pad) : stages_for(g.n_pad);
     if (t.stages > 0) g.stages = t.stages < max_stages(g.n_pad) ? t.stages : max_stages(g.n_pad);
     g.hpc = 1;
     if (t.hpc > 0) g.hpc = t.hpc < max_heads_per_cta(g.n_pad) ? t.hpc : max_heads_per_cta(g.n_pad);
@@ -298,7 +402,7 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(m_tiles, (n_h + g.hpc - 1) / g.hpc, (g.n_tokens + MAX_N - 1) / MAX_N);
+    lc.gridDim = dim3(m_tiles, (n_h + g.hpc - 1) / g.hpc, (g.n_tokens + g.n_tile - 1) / g.n_tile);
     lc.blockDim = dim3(NTHREADS);
     lc.dynamicSmemBytes = smem;
     lc.stream = stream;
@@ -307,7 +411,7 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = t.pdl ? 1 : 0;
-    if (cudaLaunchKernelEx(&lc, tc_gemm_kernel, a, b, g) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&lc, tc_gemm_kernel, a, b, a2, g) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
@@ -344,7 +448,7 @@ inline mla_status tc_gemm_absorb(const mla_config* c, const void* q_nope, const 
     if (!tcg::encode_2d(&ta, w_uk, hd, (uint64_t)c->d_latent, hd, tcg::BM) ||
         !tcg::encode_2d(&tb, q_nope, hd, (uint64_t)n, hd, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
-    return tcg::launch(g, ta, tb, c->d_latent / tcg::BM, c->n_heads, t, stream);
+    return tcg::launch(g, ta, tb, ta, c->d_latent / tcg::BM, c->n_heads, t, stream);
 }
 
 inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void* w_uv, void* o, int n,
@@ -361,7 +465,45 @@ inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void
     if (!tcg::encode_2d(&ta, w_uv, hd, (uint64_t)c->d_latent, hd, 64) ||
         !tcg::encode_2d(&tb, o_lat, hc, (uint64_t)n, hc, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
-    return tcg::launch(g, ta, tb, c->d_nope / tcg::BM, c->n_heads, t, stream);
+    return tcg::launch(g, ta, tb, ta, c->d_nope / tcg::BM, c->n_heads, t, stream);
+}
+
+inline bool tc_gemm_append_supported(const mla_config* c, int n, int cc_major, int cc_minor) {
+    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 && c->d_model % 64 == 0 &&
+           c->d_latent % 128 == 0 && c->d_rope > 0 && c->d_rope <= 128 && (c->d_rope * 2) % 16 == 0;
+}
+
+// mla_cache_append on the tensor cores: one CTA per (128 output columns, token tile); the
+// last column tile is W_KR, rotated and stored through shared memory.  Few tokens (decode
+// steps) use 32-token tiles so that more CTAs share the weight stream.
+inline mla_status tc_gemm_append(const mla_config* c, const mla_cache* k, const void* x, const void* w_dkv,
+                                 const void* w_kr, const int32_t* seq_idx, const int32_t* pos, int n,
+                                 const tcg::Tuning& t, cudaStream_t stream) {
+    tcg::GemmArgs g{};
+    g.mode = tcg::APPEND;
+    g.n_tokens = n;
+    g.n_tile = n <= 512 ? 32 : tcg::MAX_N;
+    g.n_pad = tcg::n_pad_for(n < g.n_tile ? n : g.n_tile);
+    g.k_chunks = c->d_model / tcg::BK;
+    g.n_h = 1;
+    g.d_c = c->d_latent;
+    g.d_r = c->d_rope;
+    g.width = c->d_latent + c->d_rope;
+    g.pos = pos;
+    rope_freq_fill(&g.rf, c->d_rope, c->rope_base);
+    g.pool = k->pool;
+    g.page_table = k->page_table;
+    g.seq_idx = seq_idx;
+    g.max_pages = k->max_pages;
+    g.batch = k->batch;
+    g.page_size = c->page_size;
+    g.num_pages = k->num_pages;
+    CUtensorMap ta, ta2, tb;
+    if (!tcg::encode_2d(&ta, w_dkv, (uint64_t)c->d_latent, (uint64_t)c->d_model, (uint64_t)c->d_latent, 64) ||
+        !tcg::encode_2d(&ta2, w_kr, (uint64_t)c->d_rope, (uint64_t)c->d_model, (uint64_t)c->d_rope, 64) ||
+        !tcg::encode_2d(&tb, x, (uint64_t)c->d_model, (uint64_t)n, (uint64_t)c->d_model, (uint32_t)g.n_pad))
+        return MLA_ERR_CUDA;
+    return tcg::launch(g, ta, tb, ta2, c->d_latent / tcg::BM + 1, 1, t, stream);
 }
 
 }  // namespace mla
