@@ -35,9 +35,10 @@
  *   - Kernels are launched with programmatic dependent launch: a kernel of this library may
  *     start while the kernel before it in the stream finishes, if that kernel allows it
  *     (griddepcontrol.launch_dependents; the library's own kernels do).  It waits for that
- *     kernel before reading what that kernel may write: q_cat in mla_decode / mla_prefill
- *     (written by mla_absorb_q), o_lat in mla_out, q_nope / q_rope / pos in mla_absorb_q.
- *     The cache, page table and lengths are read without that wait, so they must be produced
+ *     kernel before reading what that kernel may write: q_cat and the cache rows in
+ *     mla_decode / mla_prefill (written by mla_absorb_q and mla_cache_append), o_lat in
+ *     mla_out, q_nope / q_rope / pos and x in mla_absorb_q and mla_cache_append.  The page
+ *     table and lengths are read without the wait, so they must be produced
  *     by work that completes before the preceding kernel starts (ordinary kernels and copies
  *     do; MLA_TUNE_NO_PDL turns programmatic launch off).
  *
@@ -202,7 +203,8 @@ typedef enum {
     MLA_TUNE_GEMM_HEADS = 3,   /* >0: heads per CTA of the tcgen05 projection GEMMs          */
     MLA_TUNE_GEMM_STAGES = 4,  /* >0: ring depth of the tcgen05 projection GEMMs             */
     MLA_TUNE_NO_PDL = 5,       /* 1: launch without programmatic dependent launch            */
-    MLA_TUNE_SCHEDULE = 6      /* split schedule: 0 automatic, 1 flat page partition only     */
+    MLA_TUNE_SCHEDULE = 6,     /* split schedule: 0 automatic, 1 flat page partition only     */
+    MLA_TUNE_GEMM_KSPLIT = 7   /* >0: K split (cluster size, <= 8) of the tcgen05 GEMMs      */
 } mla_tuning_key;
 MLA_API int32_t mla_set_tuning(int32_t key, int32_t value);
 

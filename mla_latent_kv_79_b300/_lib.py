@@ -16,6 +16,7 @@ MLA_STATIC_SCRATCH_BYTES = 80 << 20
 MLA_F32, MLA_BF16 = 0, 1
 MLA_TUNE_ATTN_UNITS, MLA_TUNE_FORCE_SIMT, MLA_TUNE_WAIT_LIMIT_US = 0, 1, 2
 MLA_TUNE_GEMM_HEADS, MLA_TUNE_GEMM_STAGES, MLA_TUNE_NO_PDL, MLA_TUNE_SCHEDULE = 3, 4, 5, 6
+MLA_TUNE_GEMM_KSPLIT = 7
 
 
 class MlaConfig(ctypes.Structure):

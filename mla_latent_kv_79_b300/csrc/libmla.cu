@@ -59,7 +59,7 @@ static mla_status device_info(DeviceInfo** out) {
 }
 
 // ----------------------------------------------------------------------------- knobs
-static std::atomic<int> g_tune[7] = {{0}, {0}, {2000000}, {0}, {0}, {0}, {0}};
+static std::atomic<int> g_tune[8] = {{0}, {0}, {2000000}, {0}, {0}, {0}, {0}, {0}};
 static thread_local int g_last_path = 0;
 static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 static std::atomic<unsigned long long> g_launches{0};
@@ -112,6 +112,7 @@ static tcg::Tuning gemm_tuning(unsigned long long wait_ns) {
     t.wait_ns = wait_ns;
     t.hpc = g_tune[MLA_TUNE_GEMM_HEADS].load();
     t.stages = g_tune[MLA_TUNE_GEMM_STAGES].load();
+    t.ksplit = g_tune[MLA_TUNE_GEMM_KSPLIT].load();
     t.pdl = g_tune[MLA_TUNE_NO_PDL].load() == 0;
     return t;
 }
@@ -228,7 +229,7 @@ const char* mla_status_string(mla_status s) {
 }
 
 int32_t mla_set_tuning(int32_t key, int32_t value) {
-    if (key < 0 || key > 6) return -1;
+    if (key < 0 || key > 7) return -1;
     if (key == MLA_TUNE_WAIT_LIMIT_US && value <= 0) value = 2000000;
     return g_tune[key].exchange(value);
 }

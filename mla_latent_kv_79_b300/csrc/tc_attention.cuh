@@ -149,24 +149,15 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
     const uint32_t stage_bytes = (uint32_t)(nch * CHUNK);
     bool waited = false;
     while (ok && c.next(a.qs, &sg)) {
-        int pg0 = sg.page_begin;
-        bool early = false;  // this segment's first page went out before the query
-        if (rank == 0 && !waited) {
-            // The query is the one input written by the kernel just before (the absorption
-            // GEMM, whose dependants may start early): the unit's first page (ring item 2, a
-            // free stage) goes out before the grid-dependency wait, the query after it.
-            int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + pg0);
-            if (page < 0 || page >= a.num_pages) {
-                set_device_error(MLA_ERR_DEVICE_BOUNDS);
-                page = 0;
-            }
-            const uint32_t stage = (g + Q_ITEMS) % STAGES, fb = bar_addr(base, B_FULL + stage);
-            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-            for (int cc = 0; cc < nch; ++cc)
-                ptx::tma_load_2d(base + stage * stage_bytes + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
+        const int pg0 = sg.page_begin;
+        if (!waited) {
+            // The kernels before this one in the stream may still be running (programmatic
+            // launch): the absorption GEMM writes the queries, and an earlier cache append may
+            // not have finished either, so the first load waits for the preceding grid.
+            // (Issuing the unit's first page, or an L2 prefetch of it, before this wait
+            // measured no faster.)
             grid_dependency_wait();
             waited = true;
-            early = true;
         }
         if (rank == 0) {  // the segment's query: box b of the 18 is (columns 64*(b/2), rows 64*(b%2))
             for (int qi = 0; qi < Q_ITEMS; ++qi, ++g) {
@@ -180,10 +171,6 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                 }
             }
             if (!ok) break;
-            if (early) {  // ring item g (the first page) is already in flight
-                ++pg0;
-                ++g;
-            }
         }
         for (int pg = pg0; pg < sg.page_end; ++pg, ++g) {
             const uint32_t stage = g % STAGES;
@@ -549,10 +536,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     ptx::tc_fence_after();
     ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
-    // Launched as a programmatic dependent, this kernel may start while the one before it (the
-    // absorption GEMM) finishes.  Only the queries come from that kernel: the score CTA's
-    // producer waits for it (griddepcontrol.wait) before their loads; lengths, page table and
-    // cache come from earlier work and are read at once.
+    // Launched as a programmatic dependent, this kernel may start while the kernels before it
+    // (the absorption GEMM, and before that possibly a cache append) finish.  Lengths and page
+    // table come from earlier work and are read at once; both producers wait for the preceding
+    // grid (griddepcontrol.wait) before loading queries or cache rows.
 
     UnitCursor cur;
     long long per;

@@ -13,9 +13,10 @@
 // With few tokens (decode) a CTA's whole weight slice is in flight at once.  The kernel is
 // launched as a programmatic dependent: the weights do not depend on the previous kernel, so
 // their loads are issued before the grid-dependency wait and only the token operand after it.
-// In ABSORB mode the CTAs of the first m-tile also write the RoPE half of q_cat for their head
-// (RoPE(q_rope[n, h], pos[n]) into columns [d_c, d_c + d_r)), with the epilogue warps, which
-// are idle while the weights stream.
+// In ABSORB mode the CTAs also write the RoPE half of q_cat (RoPE(q_rope[n, h], pos[n]) into
+// columns [d_c, d_c + d_r)), spread over all CTAs of a token tile, with the epilogue warps,
+// which are idle while the weights stream.  Few tokens with a deep K (APPEND in a decode step)
+// split K over a cluster of CTAs that add their partial sums through distributed shared memory.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -26,6 +27,8 @@ namespace mla {
 namespace tcg {
 
 constexpr int BM = 128, BK = 64, MAX_N = 256, HPC = 4, MAX_STAGES = 16;
+constexpr int MAX_KSPLIT = 8;                 // portable cluster size
+constexpr int SPLIT_STAGES = 4;               // ring depth of split-K CTAs (a few share an SM)
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int NTHREADS = 192;
 constexpr int SMEM_LIMIT = 232448;            // opt-in shared memory per CTA
@@ -75,6 +78,7 @@ struct GemmArgs {
     int d_r;
     RopeFreq rf;
     int n_tile;         // tokens per CTA tile (the grid's z dimension walks them)
+    int ksplit;         // K split over a cluster of this many CTAs (1: none; > 1 needs hpc 1)
     // APPEND: the paged pool and where each token goes (pos is the token's position)
     void* pool;
     const int* page_table;
@@ -86,7 +90,7 @@ struct GemmArgs {
 // launch choices (0 = automatic), from the library's tuning knobs
 struct Tuning {
     unsigned long long wait_ns = 2000000000ull;
-    int hpc = 0, stages = 0;
+    int hpc = 0, stages = 0, ksplit = 0;
     bool pdl = true;
 };
 
@@ -105,14 +109,15 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned lo
     }
 }
 
-// Chunk c of a CTA with nh heads: head-major for ABSORB (a head's K chunks are adjacent columns
-// of W_UK), K-major for OUT (the CTA's heads are adjacent column slabs of W_UV, so one 64-row
-// block of all of them is requested together).
-__device__ __forceinline__ int chunk_head(const GemmArgs& g, int c, int nh) {
-    return g.mode == OUT ? c % nh : c / g.k_chunks;
+// Chunk c of a CTA with nh heads and kper K chunks per head: head-major for ABSORB (a head's K
+// chunks are adjacent columns of W_UK), K-major for OUT (the CTA's heads are adjacent column
+// slabs of W_UV, so one 64-row block of all of them is requested together).  chunk_k is the
+// index within the CTA's K range.
+__device__ __forceinline__ int chunk_head(const GemmArgs& g, int c, int nh, int kper) {
+    return g.mode == OUT ? c % nh : c / kper;
 }
-__device__ __forceinline__ int chunk_k(const GemmArgs& g, int c, int nh) {
-    return g.mode == OUT ? c / nh : c % g.k_chunks;
+__device__ __forceinline__ int chunk_k(const GemmArgs& g, int c, int nh, int kper) {
+    return g.mode == OUT ? c / nh : c % kper;
 }
 
 // Pool row (element offset) of appended token n, or -1 (and the bounds error) when its sequence,
@@ -131,8 +136,86 @@ __device__ __forceinline__ long long append_row(const GemmArgs& g, int n) {
     return ((long long)page * g.page_size + p % g.page_size) * g.width;
 }
 
-// grid: (m-tiles, ceil(n_h / hpc), n-tiles).  tmA2 is W_KR in APPEND mode (its m-tile is the
-// last one), otherwise unused.
+// ABSORB: the RoPE half of q_cat for the tokens of this CTA's n-tile, shared among all the
+// tile's CTAs.  The tile's (token, pair) items are cut into equal runs, one per CTA; a thread
+// takes items of its CTA's run and rotates each for a strided subset of the heads, so that the
+// cos and sin of an angle are computed once per CTA rather than once per head.  tid: 0..127.
+__device__ __forceinline__ void absorb_rope(const GemmArgs& g, int n0, int tid) {
+    const int half = g.d_r / 2;
+    const int items = min(g.n_tile, g.n_tokens - n0) * half;
+    const int ctas = (int)(gridDim.x * gridDim.y), cta = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+    const int per = (items + ctas - 1) / ctas;
+    const int p0 = cta * per, np = min(per, items - p0);
+    if (np <= 0) return;
+    const int G = np < 128 ? np : 128;   // threads per head group
+    const int HG = 128 / G, hg = tid / G;
+    if (hg >= HG) return;
+    bf16* qc = reinterpret_cast<bf16*>(g.out);
+    constexpr int BATCH = 8;  // loads in flight per thread before the first store
+    for (int q = p0 + tid % G; q < p0 + np; q += G) {
+        const int n = n0 + q / half, i = q % half;
+        float c, sn;
+        rope_cos_sin(__ldg(g.pos + n), g.rf.theta[i], &c, &sn);
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(g.q_rope + (size_t)n * g.n_h * g.d_r + 2 * i);
+        for (int h = hg; h < g.n_h; h += HG * BATCH) {
+            uint32_t x[BATCH];
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) {
+                const int hh = h + j * HG;
+                x[j] = hh < g.n_h ? __ldg(src + (size_t)hh * (g.d_r / 2)) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) {
+                const int hh = h + j * HG;
+                if (hh >= g.n_h) break;
+                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&x[j]);
+                const float x0 = __bfloat162float(v.x), x1 = __bfloat162float(v.y);
+                *reinterpret_cast<__nv_bfloat162*>(qc + ((size_t)n * g.n_h + hh) * g.width + g.d_c + 2 * i) =
+                    __floats2bfloat162_rn(x0 * c - x1 * sn, x0 * sn + x1 * c);
+            }
+        }
+    }
+}
+
+// Split K: the CTA of cluster rank ks adds the partial sums of all ksplit CTAs (in rank order,
+// so the result does not depend on timing) for its slice of the tile's tokens and stores them
+// as the mode's epilogue would.  Partials sit at the start of each CTA's shared memory as
+// [n_pad][128] fp32; tid (0..127) is the row m of the tile.
+__device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, const int* rowoff, int mt, int h0,
+                                            int n0, int ks, bool rope_tile, int tid) {
+    const int KS = g.ksplit;
+    const int n_here = min(g.n_pad, g.n_tokens - n0);
+    const int per = (n_here + KS - 1) / KS, t0 = ks * per, t1 = min(n_here, t0 + per);
+    bf16* out = reinterpret_cast<bf16*>(g.mode == APPEND ? g.pool : g.out);
+    for (int nl = t0; nl < t1; ++nl) {
+        const uint32_t a = base + (uint32_t)(nl * BM + tid) * 4u;
+        float v = 0.f;
+        for (int r = 0; r < KS; ++r) v += ptx::ld_cluster_f32(ptx::mapa(a, (uint32_t)r));
+        const int n = n0 + nl;
+        if (g.mode == ABSORB) {
+            out[((size_t)n * g.n_h + h0) * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
+        } else if (g.mode == OUT) {
+            out[(size_t)n * g.n_h * g.d_h + (size_t)h0 * g.d_h + mt * BM + tid] = __float2bfloat16_rn(v);
+        } else if (!rope_tile) {
+            if (rowoff[nl] >= 0) out[(size_t)rowoff[nl] * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
+        } else {
+            // the pair (2i, 2i+1) sits in lanes tid, tid + 1 of one warp
+            const float w = __shfl_xor_sync(0xffffffffu, v, 1);
+            if ((tid & 1) == 0 && tid < g.d_r && rowoff[nl] >= 0) {
+                const int i = tid >> 1;
+                float cs, sn;
+                rope_cos_sin(__ldg(g.pos + n), g.rf.theta[i], &cs, &sn);
+                *reinterpret_cast<__nv_bfloat162*>(out + (size_t)rowoff[nl] * g.width + g.d_c + 2 * i) =
+                    __floats2bfloat162_rn(v * cs - w * sn, v * sn + w * cs);
+            }
+        }
+    }
+}
+
+// grid: (m-tiles * ksplit, ceil(n_h / hpc), n-tiles), clusters of ksplit CTAs along x: the CTAs
+// of a cluster share an output tile and each sums its own K range; with ksplit > 1 they add
+// their partial sums through distributed shared memory and each stores a slice of the tile's
+// tokens.  tmA2 is W_KR in APPEND mode (its m-tile is the last one), otherwise unused.
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const GemmArgs g) {
@@ -146,7 +229,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // it waits for this grid before it reads what this grid writes
     launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, h0 = blockIdx.y * g.hpc, n0 = blockIdx.z * g.n_tile;
+    const int KS = g.ksplit, ks = (int)blockIdx.x % KS, mt = (int)blockIdx.x / KS;
+    const int h0 = blockIdx.y * g.hpc, n0 = blockIdx.z * g.n_tile;
+    const int kc0 = ks * g.k_chunks / KS, kper = (ks + 1) * g.k_chunks / KS - kc0;  // this CTA's K range
     const int nh = min(g.hpc, g.n_h - h0);
     const int S = g.stages, SB = stage_bytes(g.n_pad);
     const uint32_t acc_cols = tmem_cols(g.n_pad);                  // columns per head accumulator
@@ -156,7 +241,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int* rowoff = reinterpret_cast<int*>(smem + (bar_done - base) + 16);  // APPEND: [n_pad] (in units of W)
     const bool a_mn = g.mode != ABSORB;
     const bool rope_tile = g.mode == APPEND && mt * BM >= g.d_c;
-    const int total = nh * g.k_chunks;                             // chunks of this CTA, head-major
+    const int total = nh * kper;                                   // chunks of this CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -182,7 +267,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0 && lane == 0) {
         const uint32_t bytes = (uint32_t)(A_BYTES + g.n_pad * BK * 2);
         auto load_a = [&](int c, uint32_t st, uint32_t fb) {
-            const int h = h0 + chunk_head(g, c, nh), kc = chunk_k(g, c, nh);
+            const int h = h0 + chunk_head(g, c, nh, kper), kc = kc0 + chunk_k(g, c, nh, kper);
             if (g.mode == ABSORB) {
                 // W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + kc * BK, mt * BM, fb);
@@ -200,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
         auto load_b = [&](int c, uint32_t st, uint32_t fb) {
-            const int h = h0 + chunk_head(g, c, nh), kc = chunk_k(g, c, nh);
+            const int h = h0 + chunk_head(g, c, nh, kper), kc = kc0 + chunk_k(g, c, nh, kper);
             // q_nope viewed [n, n_h*d_h] (ABSORB), o_lat viewed [n, n_h*d_c] (OUT) or x [n, d_model]
             const int col = (g.mode == ABSORB ? h * g.d_h : g.mode == OUT ? h * g.d_c : 0) + kc * BK;
             ptx::tma_load_2d(st + A_BYTES, &tmB, col, n0, fb);
@@ -224,11 +309,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == 1 && lane == 0) {
         const uint32_t idesc = ptx::idesc_bf16(BM, g.n_pad, a_mn, false);
         for (int c = 0; c < total; ++c) {
-            const int s = c % S, kc = chunk_k(g, c, nh);
+            const int s = c % S, kc = chunk_k(g, c, nh, kper);
             if (!gwait(bar_full + 8 * s, (c / S) & 1u, g.wait_ns)) break;
             ptx::tc_fence_after();
             const uint32_t st = base + s * SB;
-            const uint32_t d = tmem + (uint32_t)chunk_head(g, c, nh) * acc_cols;
+            const uint32_t d = tmem + (uint32_t)chunk_head(g, c, nh, kper) * acc_cols;
             const uint64_t da = a_mn ? ptx::desc_sw128(st, BK * 128, 1024) : ptx::desc_sw128(st, 16, 1024);
             const uint64_t db = ptx::desc_sw128(st + A_BYTES, 16, 1024);
 #pragma unroll
@@ -243,24 +328,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;  // m within the tile
-        if (g.mode == ABSORB && mt == 0 && g.q_rope) {
+        if (g.mode == ABSORB && g.q_rope) {
             grid_dependency_wait();  // q_rope and pos come from earlier kernels
-            const int half = g.d_r / 2, tid = threadIdx.x - 64;
-            const int n_here = min(g.n_pad, g.n_tokens - n0);
-            bf16* qc = reinterpret_cast<bf16*>(g.out);
-            for (int j = 0; j < nh; ++j) {
-                const int h = h0 + j;
-                for (int e = tid; e < n_here * half; e += NTHREADS - 64) {
-                    const int n = n0 + e / half, i = e % half;
-                    float c, sn;
-                    rope_cos_sin(__ldg(g.pos + n), g.rf.theta[i], &c, &sn);
-                    const __nv_bfloat162 x =
-                        *reinterpret_cast<const __nv_bfloat162*>(g.q_rope + ((size_t)n * g.n_h + h) * g.d_r + 2 * i);
-                    const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
-                    *reinterpret_cast<__nv_bfloat162*>(qc + ((size_t)n * g.n_h + h) * g.width + g.d_c + 2 * i) =
-                        __floats2bfloat162_rn(x0 * c - x1 * sn, x0 * sn + x1 * c);
-                }
-            }
+            absorb_rope(g, n0, threadIdx.x - 64);
         }
         const int tid = threadIdx.x - 64, n_here = min(g.n_pad, g.n_tokens - n0);
         if (g.mode == APPEND) {
@@ -274,7 +344,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         // the four epilogue warps agree on the outcome of the wait (they meet at named barriers)
         bool done_ok = false;
-        if (g.mode == APPEND) {
+        if (g.mode == APPEND || KS > 1) {
             const bool mine = gwait(bar_done, 0, g.wait_ns);
             uint32_t all;
             asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
@@ -284,7 +354,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          : "memory");
             done_ok = all != 0;
         }
-        if (g.mode == APPEND && done_ok) {
+        if (KS > 1) {
+            // this CTA's partial sums, [n_pad][128] fp32, into the ring (idle: every MMA is done)
+            if (done_ok) {
+                ptx::tc_fence_after();
+                float* stg = reinterpret_cast<float*>(smem);
+                const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
+                for (int c0 = 0; c0 < g.n_pad; c0 += 32) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(taddr + c0, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < g.n_pad) stg[(c0 + i) * BM + row] = __uint_as_float(r[i]);
+                }
+            }
+        } else if (g.mode == APPEND && done_ok) {
             ptx::tc_fence_after();
             bf16* pool = reinterpret_cast<bf16*>(g.pool);
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
@@ -352,6 +437,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     }
+    if (KS > 1) {
+        // every thread of the cluster passes both barriers, whatever its waits returned
+        __syncwarp();
+        ptx::cluster_sync();  // all partial sums are staged
+        if (warp >= 2) split_store(g, base, rowoff, mt, h0, n0, ks, rope_tile, threadIdx.x - 64);
+        __syncwarp();
+        ptx::cluster_sync();  // the peers have finished reading this CTA's shared memory
+    }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -393,24 +486,53 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     GemmArgs g = g0;
     g.wait_ns = t.wait_ns;
     if (g.n_tile == 0) g.n_tile = MAX_N;
-    // APPEND streams K = d_model in 64-wide chunks per CTA: as deep a ring as fits
-    g.stages = g.mode == APPEND ? max_stages(g.n_pad) : stages_for(g.n_pad);
-    if (t.stages > 0) g.stages = t.stages < max_stages(g.n_pad) ? t.stages : max_stages(g.n_pad);
     g.hpc = 1;
     if (t.hpc > 0) g.hpc = t.hpc < max_heads_per_cta(g.n_pad) ? t.hpc : max_heads_per_cta(g.n_pad);
+    // K split over a cluster: by default for APPEND with small token tiles (a decode step's few
+    // tokens leave only a handful of CTAs, each streaming K = d_model)
+    int ksp = t.ksplit > 0 ? t.ksplit : (g.mode == APPEND && g.n_tile <= 32 ? MAX_KSPLIT : 1);
+    if (ksp > MAX_KSPLIT) ksp = MAX_KSPLIT;
+    if (ksp > g.k_chunks) ksp = g.k_chunks;
+    if (g.hpc != 1 || ksp < 1) ksp = 1;
+    g.ksplit = ksp;
+    // ring depth: APPEND without a split streams K = d_model per CTA, as deep a ring as fits;
+    // never deeper than the chunks one CTA streams; with a split, deep enough to stage the
+    // partial sums ([n_pad][128] fp32) where the ring was
+    const int chunks = g.hpc * ((g.k_chunks + ksp - 1) / ksp), mx = max_stages(g.n_pad);
+    int S = ksp > 1 ? SPLIT_STAGES : g.mode == APPEND ? mx : stages_for(g.n_pad);
+    if (t.stages > 0) S = t.stages;
+    if (S > chunks) S = chunks;
+    if (ksp > 1) {
+        const int need = (g.n_pad * BM * 4 + stage_bytes(g.n_pad) - 1) / stage_bytes(g.n_pad);
+        if (S < need) S = need;
+    }
+    if (S > mx) S = mx;
+    if (S < 1 || (ksp > 1 && S * stage_bytes(g.n_pad) < g.n_pad * BM * 4)) return MLA_ERR_UNSUPPORTED;
+    g.stages = S;
     const int smem = smem_bytes(g.n_pad, g.stages);
     if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(m_tiles, (n_h + g.hpc - 1) / g.hpc, (g.n_tokens + g.n_tile - 1) / g.n_tile);
+    lc.gridDim = dim3(m_tiles * ksp, (n_h + g.hpc - 1) / g.hpc, (g.n_tokens + g.n_tile - 1) / g.n_tile);
     lc.blockDim = dim3(NTHREADS);
     lc.dynamicSmemBytes = smem;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (t.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (ksp > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)ksp;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     lc.attrs = attr;
-    lc.numAttrs = t.pdl ? 1 : 0;
+    lc.numAttrs = na;
     if (cudaLaunchKernelEx(&lc, tc_gemm_kernel, a, b, a2, g) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
@@ -475,7 +597,8 @@ inline bool tc_gemm_append_supported(const mla_config* c, int n, int cc_major, i
 
 // mla_cache_append on the tensor cores: one CTA per (128 output columns, token tile); the
 // last column tile is W_KR, rotated and stored through shared memory.  Few tokens (decode
-// steps) use 32-token tiles so that more CTAs share the weight stream.
+// steps) use 32-token tiles and split K over clusters of 8 CTAs, so that many CTAs share the
+// weight stream.
 inline mla_status tc_gemm_append(const mla_config* c, const mla_cache* k, const void* x, const void* w_dkv,
                                  const void* w_kr, const int32_t* seq_idx, const int32_t* pos, int n,
                                  const tcg::Tuning& t, cudaStream_t stream) {

@@ -162,6 +162,60 @@ def test_out_matches_oracle(path, dtype, shape, n):
     assert rel(host(out.t), ref) <= tol(dtype)[0]
 
 
+@pytest.mark.parametrize("ksplit,stages", [(1, 0), (2, 0), (3, 0), (8, 2)])
+def test_gemm_k_split_matches_oracle(ksplit, stages):
+    """The tcgen05 GEMMs with K split over a cluster forced to uneven splits (W_UV's 8 K chunks
+    in 3 parts, d_model's 80 in 3 or 8), and with the split turned off (1) for a decode-sized
+    append: every mode's result is the oracle's whatever the split."""
+    M.mla_set_tuning(_lib.MLA_TUNE_FORCE_SIMT, 0)
+    old_k = M.mla_set_tuning(_lib.MLA_TUNE_GEMM_KSPLIT, ksplit)
+    old_s = M.mla_set_tuning(_lib.MLA_TUNE_GEMM_STAGES, stages)
+    try:
+        r = np.random.default_rng(47)
+        cfg = cfg_of(DS, "bf16")
+        n = 45
+        # absorb
+        case = W.make_decode_case(DS, "bf16", [1] * n, seed=48)
+        pos = r.integers(0, 100000, size=n).astype(np.int32)
+        q_cat = Guarded((n, DS.n_heads, DS.width), cfg.torch_dtype)
+        M.mla_absorb_q(cfg, dev(case["q_nope"]), dev(case["q_rope"]), i32(pos), dev(case["w_uk"]), q_cat=q_cat.t)
+        # out
+        o_lat = W.quantise(W.normal(r, (n, DS.n_heads, DS.d_latent)), "bf16")
+        w_uv = W.weight(r, DS.d_latent, DS.n_heads * DS.d_nope, "bf16")
+        o = Guarded((n, DS.n_heads * DS.d_nope), cfg.torch_dtype)
+        M.mla_out(cfg, dev(o_lat), dev(w_uv), o=o.t)
+        # append: one token per sequence at ragged positions
+        lens = r.integers(1, 200, size=n)
+        pt, n_pages = W.make_page_table(r, [int(l) + 1 for l in lens], DS.page_size, 2, True)
+        pool0 = W.empty_pool(n_pages, DS, "bf16")
+        cache = M.PagedCache(dev(pool0), i32(pt), i32(lens + 1))
+        x = W.quantise(W.normal(r, (n, DS.d_model)), "bf16")
+        wd = W.weight(r, DS.d_model, DS.d_latent, "bf16")
+        wk = W.weight(r, DS.d_model, DS.d_rope, "bf16")
+        M.mla_cache_append(cfg, cache, dev(x), dev(wd), dev(wk), i32(np.arange(n)), i32(lens))
+        torch.cuda.synchronize()
+        assert_no_device_error()
+        q_cat.check()
+        o.check()
+        ref = O.absorb_query(f64(case["q_nope"]), f64(case["q_rope"]), pos, f64(case["w_uk"]), DS.rope_base)
+        got = host(q_cat.t)
+        assert rel(got[..., :DS.d_latent], ref[..., :DS.d_latent]) <= TOL_OUT_BF16
+        assert rel(got[..., DS.d_latent:], ref[..., DS.d_latent:]) <= TOL_OUT_BF16
+        assert rel(host(o.t), O.up_project_output(f64(o_lat), f64(w_uv))) <= TOL_OUT_BF16
+        got_pool = host(cache.pool)
+        c_ref, k_ref = O.latent_kv(f64(x), f64(wd), f64(wk), lens, DS.rope_base)
+        written = np.zeros(got_pool.shape[:2], bool)
+        for b in range(n):
+            page, slot = pt[b, lens[b] // DS.page_size], lens[b] % DS.page_size
+            written[page, slot] = True
+            assert rel(got_pool[page, slot, :DS.d_latent], c_ref[b]) <= TOL_OUT_BF16, b
+            assert rel(got_pool[page, slot, DS.d_latent:], k_ref[b]) <= TOL_OUT_BF16, b
+        assert np.array_equal(got_pool[~written], f64(pool0)[~written])
+    finally:
+        M.mla_set_tuning(_lib.MLA_TUNE_GEMM_KSPLIT, old_k)
+        M.mla_set_tuning(_lib.MLA_TUNE_GEMM_STAGES, old_s)
+
+
 # ----------------------------------------------------------------------------------- decode
 
 DECODE_LENS = [1, 63, 64, 65, 300, 1000, 2049, 130]
