@@ -46,7 +46,8 @@ static mla_status device_info(DeviceInfo** out) {
                 (const void*)rope_query_kernel<bf16>, (const void*)rope_query_kernel<float>,
                 (const void*)simt_attention_kernel<bf16>, (const void*)simt_attention_kernel<float>,
                 (const void*)combine_kernel<bf16>, (const void*)combine_kernel<float>,
-                (const void*)tca::tc_attention_kernel, (const void*)tcg::tc_gemm_kernel};
+                (const void*)tca::tc_attention_kernel, (const void*)tcg::tc_gemm_kernel<tcg::ABSORB>,
+                (const void*)tcg::tc_gemm_kernel<tcg::OUT>, (const void*)tcg::tc_gemm_kernel<tcg::APPEND>};
             for (const void* f : fns)
                 if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)

@@ -113,11 +113,13 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned lo
 // chunks are adjacent columns of W_UK), K-major for OUT (the CTA's heads are adjacent column
 // slabs of W_UV, so one 64-row block of all of them is requested together).  chunk_k is the
 // index within the CTA's K range.
-__device__ __forceinline__ int chunk_head(const GemmArgs& g, int c, int nh, int kper) {
-    return g.mode == OUT ? c % nh : c / kper;
+template <int MODE>
+__device__ __forceinline__ int chunk_head(int c, int nh, int kper) {
+    return MODE == OUT ? c % nh : c / kper;
 }
-__device__ __forceinline__ int chunk_k(const GemmArgs& g, int c, int nh, int kper) {
-    return g.mode == OUT ? c / nh : c % kper;
+template <int MODE>
+__device__ __forceinline__ int chunk_k(int c, int nh, int kper) {
+    return MODE == OUT ? c / nh : c % kper;
 }
 
 // Pool row (element offset) of appended token n, or -1 (and the bounds error) when its sequence,
@@ -181,20 +183,21 @@ __device__ __forceinline__ void absorb_rope(const GemmArgs& g, int n0, int tid) 
 // so the result does not depend on timing) for its slice of the tile's tokens and stores them
 // as the mode's epilogue would.  Partials sit at the start of each CTA's shared memory as
 // [n_pad][128] fp32; tid (0..127) is the row m of the tile.
+template <int MODE>
 __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, const int* rowoff, int mt, int h0,
                                             int n0, int ks, bool rope_tile, int tid) {
     const int KS = g.ksplit;
     const int n_here = min(g.n_pad, g.n_tokens - n0);
     const int per = (n_here + KS - 1) / KS, t0 = ks * per, t1 = min(n_here, t0 + per);
-    bf16* out = reinterpret_cast<bf16*>(g.mode == APPEND ? g.pool : g.out);
+    bf16* out = reinterpret_cast<bf16*>(MODE == APPEND ? g.pool : g.out);
     for (int nl = t0; nl < t1; ++nl) {
         const uint32_t a = base + (uint32_t)(nl * BM + tid) * 4u;
         float v = 0.f;
         for (int r = 0; r < KS; ++r) v += ptx::ld_cluster_f32(ptx::mapa(a, (uint32_t)r));
         const int n = n0 + nl;
-        if (g.mode == ABSORB) {
+        if (MODE == ABSORB) {
             out[((size_t)n * g.n_h + h0) * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
-        } else if (g.mode == OUT) {
+        } else if (MODE == OUT) {
             out[(size_t)n * g.n_h * g.d_h + (size_t)h0 * g.d_h + mt * BM + tid] = __float2bfloat16_rn(v);
         } else if (!rope_tile) {
             if (rowoff[nl] >= 0) out[(size_t)rowoff[nl] * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
@@ -216,6 +219,7 @@ __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, co
 // of a cluster share an output tile and each sums its own K range; with ksplit > 1 they add
 // their partial sums through distributed shared memory and each stores a slice of the tile's
 // tokens.  tmA2 is W_KR in APPEND mode (its m-tile is the last one), otherwise unused.
+template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const GemmArgs g) {
@@ -239,8 +243,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t bar_full = base + S * SB, bar_empty = bar_full + 8 * S, bar_done = bar_empty + 8 * S;
     const uint32_t slot = bar_done + 8;
     int* rowoff = reinterpret_cast<int*>(smem + (bar_done - base) + 16);  // APPEND: [n_pad] (in units of W)
-    const bool a_mn = g.mode != ABSORB;
-    const bool rope_tile = g.mode == APPEND && mt * BM >= g.d_c;
+    const bool a_mn = MODE != ABSORB;
+    const bool rope_tile = MODE == APPEND && mt * BM >= g.d_c;
     const int total = nh * kper;                                   // chunks of this CTA
 
     if (threadIdx.x == 0) {
@@ -267,11 +271,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0 && lane == 0) {
         const uint32_t bytes = (uint32_t)(A_BYTES + g.n_pad * BK * 2);
         auto load_a = [&](int c, uint32_t st, uint32_t fb) {
-            const int h = h0 + chunk_head(g, c, nh, kper), kc = kc0 + chunk_k(g, c, nh, kper);
-            if (g.mode == ABSORB) {
+            const int h = h0 + chunk_head<MODE>(c, nh, kper), kc = kc0 + chunk_k<MODE>(c, nh, kper);
+            if (MODE == ABSORB) {
                 // W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + kc * BK, mt * BM, fb);
-            } else if (g.mode == APPEND) {
+            } else if (MODE == APPEND) {
                 // W_DKV (or, for the last tile, W_KR) rows k in [kc*64, +64) x output columns
                 // m .. m + 128 (MN-major, two boxes; columns past d_r read as zeros)
                 const CUtensorMap* t = rope_tile ? &tmA2 : &tmA;
@@ -285,9 +289,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
         auto load_b = [&](int c, uint32_t st, uint32_t fb) {
-            const int h = h0 + chunk_head(g, c, nh, kper), kc = kc0 + chunk_k(g, c, nh, kper);
+            const int h = h0 + chunk_head<MODE>(c, nh, kper), kc = kc0 + chunk_k<MODE>(c, nh, kper);
             // q_nope viewed [n, n_h*d_h] (ABSORB), o_lat viewed [n, n_h*d_c] (OUT) or x [n, d_model]
-            const int col = (g.mode == ABSORB ? h * g.d_h : g.mode == OUT ? h * g.d_c : 0) + kc * BK;
+            const int col = (MODE == ABSORB ? h * g.d_h : MODE == OUT ? h * g.d_c : 0) + kc * BK;
             ptx::tma_load_2d(st + A_BYTES, &tmB, col, n0, fb);
         };
         // the first ring's worth of weights goes out before the previous kernel has finished
@@ -309,11 +313,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == 1 && lane == 0) {
         const uint32_t idesc = ptx::idesc_bf16(BM, g.n_pad, a_mn, false);
         for (int c = 0; c < total; ++c) {
-            const int s = c % S, kc = chunk_k(g, c, nh, kper);
+            const int s = c % S, kc = chunk_k<MODE>(c, nh, kper);
             if (!gwait(bar_full + 8 * s, (c / S) & 1u, g.wait_ns)) break;
             ptx::tc_fence_after();
             const uint32_t st = base + s * SB;
-            const uint32_t d = tmem + (uint32_t)chunk_head(g, c, nh, kper) * acc_cols;
+            const uint32_t d = tmem + (uint32_t)chunk_head<MODE>(c, nh, kper) * acc_cols;
             const uint64_t da = a_mn ? ptx::desc_sw128(st, BK * 128, 1024) : ptx::desc_sw128(st, 16, 1024);
             const uint64_t db = ptx::desc_sw128(st + A_BYTES, 16, 1024);
 #pragma unroll
@@ -328,12 +332,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;  // m within the tile
-        if (g.mode == ABSORB && g.q_rope) {
+        if (MODE == ABSORB && g.q_rope) {
             grid_dependency_wait();  // q_rope and pos come from earlier kernels
             absorb_rope(g, n0, threadIdx.x - 64);
         }
         const int tid = threadIdx.x - 64, n_here = min(g.n_pad, g.n_tokens - n0);
-        if (g.mode == APPEND) {
+        if (MODE == APPEND) {
             // where each token of the tile goes (inputs of earlier kernels: after the wait)
             grid_dependency_wait();
             for (int i = tid; i < n_here; i += NTHREADS - 64) {
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         // the four epilogue warps agree on the outcome of the wait (they meet at named barriers)
         bool done_ok = false;
-        if (g.mode == APPEND || KS > 1) {
+        if (MODE == APPEND || KS > 1) {
             const bool mine = gwait(bar_done, 0, g.wait_ns);
             uint32_t all;
             asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         if (c0 + i < g.n_pad) stg[(c0 + i) * BM + row] = __uint_as_float(r[i]);
                 }
             }
-        } else if (g.mode == APPEND && done_ok) {
+        } else if (MODE == APPEND && done_ok) {
             ptx::tc_fence_after();
             bf16* pool = reinterpret_cast<bf16*>(g.pool);
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         __floats2bfloat162_rn(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
                 }
             }
-        } else if (g.mode != APPEND && gwait(bar_done, 0, g.wait_ns)) {
+        } else if (MODE != APPEND && gwait(bar_done, 0, g.wait_ns)) {
             ptx::tc_fence_after();
             bf16* out = reinterpret_cast<bf16*>(g.out);
             for (int j = 0; j < nh; ++j) {
@@ -427,7 +431,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int n = n0 + c0 + i;
                         if (c0 + i < g.n_pad && n < g.n_tokens) {
                             const bf16 v = __float2bfloat16_rn(__uint_as_float(r[i]));
-                            if (g.mode == ABSORB)
+                            if (MODE == ABSORB)
                                 out[((size_t)n * g.n_h + h) * g.width + mt * BM + row] = v;
                             else
                                 out[(size_t)n * g.n_h * g.d_h + (size_t)h * g.d_h + mt * BM + row] = v;
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // every thread of the cluster passes both barriers, whatever its waits returned
         __syncwarp();
         ptx::cluster_sync();  // all partial sums are staged
-        if (warp >= 2) split_store(g, base, rowoff, mt, h0, n0, ks, rope_tile, threadIdx.x - 64);
+        if (warp >= 2) split_store<MODE>(g, base, rowoff, mt, h0, n0, ks, rope_tile, threadIdx.x - 64);
         __syncwarp();
         ptx::cluster_sync();  // the peers have finished reading this CTA's shared memory
     }
@@ -510,7 +514,11 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     if (S < 1 || (ksp > 1 && S * stage_bytes(g.n_pad) < g.n_pad * BM * 4)) return MLA_ERR_UNSUPPORTED;
     g.stages = S;
     const int smem = smem_bytes(g.n_pad, g.stages);
-    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    // one instantiation per mode: each launch fetches only its own code (cold after every L2
+    // flush; instruction fetch stalls dominated this short kernel when the modes shared one)
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs) =
+        g.mode == ABSORB ? tc_gemm_kernel<ABSORB> : g.mode == OUT ? tc_gemm_kernel<OUT> : tc_gemm_kernel<APPEND>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(m_tiles * ksp, (n_h + g.hpc - 1) / g.hpc, (g.n_tokens + g.n_tile - 1) / g.n_tile);
@@ -533,7 +541,7 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     }
     lc.attrs = attr;
     lc.numAttrs = na;
-    if (cudaLaunchKernelEx(&lc, tc_gemm_kernel, a, b, a2, g) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&lc, kern, a, b, a2, g) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
