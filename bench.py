@@ -271,15 +271,15 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(qn=q_nope, qr=q_rope, xx=None, oo=o, ll=lse):
         if appending:  # the same positions every step: the cache ends each step identical
-            M.mla_cache_append(cfg, cache, x, w_dkv, w_kr, a_seq, a_pos, stream=stream)
-        M.mla_absorb_q(cfg, q_nope, q_rope, pos, w_uk, q_cat=q_cat, stream=stream)
+            M.mla_cache_append(cfg, cache, x if xx is None else xx, w_dkv, w_kr, a_seq, a_pos, stream=stream)
+        M.mla_absorb_q(cfg, qn, qr, pos, w_uk, q_cat=q_cat, stream=stream)
         if prefill:
-            M.mla_prefill(cfg, cache, 0, 0, q_cat, o_lat=o_lat, lse=lse, workspace=ws, stream=stream)
+            M.mla_prefill(cfg, cache, 0, 0, q_cat, o_lat=o_lat, lse=ll, workspace=ws, stream=stream)
         else:
-            M.mla_decode(cfg, cache, q_cat, o_lat=o_lat, lse=lse, workspace=ws, stream=stream)
-        M.mla_out(cfg, o_lat, w_uv, o=o, stream=stream)
+            M.mla_decode(cfg, cache, q_cat, o_lat=o_lat, lse=ll, workspace=ws, stream=stream)
+        M.mla_out(cfg, o_lat, w_uv, o=oo, stream=stream)
 
     warm = max(3, args.warmup)
     clocks = ClockSampler(local)
@@ -326,13 +326,26 @@ def run_ours(args):
     path = M.mla_last_attention_path()
     assert M.mla_get_device_error() == 0
 
-    # end to end through host buffers: per step, copy the step's queries in from pinned
-    # host memory and read the output back
-    h_qn = q_nope.cpu().pin_memory()
-    h_qr = q_rope.cpu().pin_memory()
-    h_x = x.cpu().pin_memory() if appending else None
-    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    # end to end through host buffers: per step, the step's inputs come in from pinned host
+    # memory in one copy and its results go back in one copy (the device tensors the path reads
+    # and writes are views of one staging buffer each way, as a serving loop would pack them)
+    def staging(tensors, pinned):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 15) // 16 * 16
+        buf = torch.empty(n, dtype=torch.uint8, device="cpu" if pinned else "cuda")
+        if pinned:
+            buf = buf.pin_memory()
+        views = [buf[o_:o_ + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o_, t in zip(offs, tensors)]
+        return buf, views
+    ins = [q_nope, q_rope] + ([x] if appending else [])
+    d_in, e_in = staging(ins, pinned=False)
+    h_in, h_in_views = staging(ins, pinned=True)
+    for hv, t in zip(h_in_views, ins):
+        hv.copy_(t)
+    d_out, (e_o, e_lse) = staging([o, lse], pinned=False)
+    h_out, _ = staging([o, lse], pinned=True)
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         dist.barrier()
@@ -340,13 +353,9 @@ def run_ours(args):
     for i in range(K):
         flush.zero_()
         eev[i][0].record(stream)
-        q_nope.copy_(h_qn, non_blocking=True)
-        q_rope.copy_(h_qr, non_blocking=True)
-        if appending:
-            x.copy_(h_x, non_blocking=True)
-        step()
-        h_o.copy_(o, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        step(e_in[0], e_in[1], e_in[2] if appending else None, e_o, e_lse)
+        h_out.copy_(d_out, non_blocking=True)
         eev[i][1].record(stream)
     torch.cuda.synchronize()
     clock = clocks.stop()
@@ -388,10 +397,8 @@ def run_ours(args):
                      "tflops": alg_flops / k_mean_s / 1e12, "peak_source": src,
                      "tensor_frac": alg_flops / k_mean_s / 1e12 / tflops,
                      "roofline_us": 1e6 * max(alg_bytes / (hbm * 1e9), alg_flops / (tflops * 1e12))},
-        "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size()
-                                          + (h_x.numel() * h_x.element_size() if appending else 0)),
-                "d2h_bytes_per_step": int(h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size())},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h_in.numel()),
+                "d2h_bytes_per_step": int(h_out.numel())},
         "gpu_launches": int(launches),
         "clocks": clock,
         "cpu_baseline": None,
