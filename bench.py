@@ -63,17 +63,26 @@ def workload_numbers(case):
     return bytes_, flops
 
 
-def source_digest():
+# the sources each profiled kernel is compiled from (its own header and the headers it includes)
+KERNEL_SOURCES = {
+    "tc_attention": ["tc_attention.cuh", "tc_ptx.cuh", "sched.cuh", "mla_common.cuh", "simt_attention.cuh"],
+    "simt_attention": ["simt_attention.cuh", "sched.cuh", "mla_common.cuh"],
+    "tc_gemm": ["tc_gemm.cuh", "tc_ptx.cuh", "mla_common.cuh"],
+}
+
+
+def source_digest(kernel_key=None):
+    """Digest of a kernel's sources (all of csrc/ when kernel_key is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_79_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES.get(kernel_key) or sorted(os.listdir(csrc)):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_key: str, workload: str):
     """DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed
-    ncu summary profiles/<kernel>_<workload>.md, or None when it is missing or the kernel
+    ncu summary profiles/<kernel>_<workload>.md, or None when it is missing or the kernel's
     sources changed since that capture (the summary records their digest)."""
     p = os.path.join(PROFILE_DIR, f"{kernel_key}_{workload}.md")
     if not os.path.exists(p):
@@ -84,7 +93,7 @@ def ncu_traffic(kernel_key: str, workload: str):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip().strip("`")] = v.strip().strip("`")
-    if fields.get("source_digest") != source_digest():
+    if (fields.get("source_digest", "").split() or [""])[0] != source_digest(kernel_key):
         return None
     try:
         return int(fields["dram_bytes_per_launch"])
@@ -154,22 +163,26 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------ reference arm
 
-def cpu_oracle_sample(case, n_seq: int):
+def cpu_oracle_sample(case, n_seq: int, out_proj: bool = False):
     """Time the float64 oracle (un-absorbed: restore K and V, softmax attention, W_UV folded
-    in by V) on the first n_seq sequences with all heads.  Returns seconds."""
+    in by V, and W_O when out_proj) on the first n_seq sequences with all heads.  Returns
+    seconds."""
     import oracle.mla_oracle as O
     s = case["shape"]
     sc = O.default_scale(s.d_nope, s.d_rope)
     pool = case["pool"]
     f = lambda a: W.to_f64(a, case["dtype"])  # noqa: E731
     w_uk, w_uv = f(case["w_uk"]), f(case["w_uv"])
+    w_o = f(case["w_o"]) if out_proj else None
     t0 = time.perf_counter()
     for b in range(n_seq):
         L = int(case["seq_lens"][b])
         rows = W.to_f64(W.gather_rows(pool, case["page_table"][b], L), case["dtype"])
         q_r = O.rope_rotate(f(case["q_rope"][b]), case["pos"][b], s.rope_base)
-        O.attention_unabsorbed(f(case["q_nope"][b]), q_r, rows[:, :s.d_latent], rows[:, s.d_latent:],
-                               w_uk, w_uv, sc)
+        o = O.attention_unabsorbed(f(case["q_nope"][b]), q_r, rows[:, :s.d_latent], rows[:, s.d_latent:],
+                                   w_uk, w_uv, sc)[0]
+        if out_proj:
+            O.output_projection(o.reshape(1, -1), w_o)
     return time.perf_counter() - t0
 
 
@@ -190,15 +203,15 @@ def run_reference(args):
         return 0
     case = W.make_workload(args.workload)
     for _ in range(max(0, args.warmup)):
-        cpu_oracle_sample(case, 1)
-    ts = [cpu_oracle_sample(case, 1) for _ in range(args.steps)]
+        cpu_oracle_sample(case, 1, args.out_proj)
+    ts = [cpu_oracle_sample(case, 1, args.out_proj) for _ in range(args.steps)]
     t = sum(ts)
     value = args.steps / t
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(args.workload, case),
+        "data": "synthetic", "config": config_of(args.workload, case, args.out_proj),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
                          "sample": "one sequence (4096 cached tokens, all 128 heads) per step, "
                                    "un-absorbed float64 oracle"},
@@ -208,12 +221,13 @@ def run_reference(args):
     return 0
 
 
-def config_of(name, case):
+def config_of(name, case, out_proj=False):
     s = case["shape"]
     w = W.WORKLOADS[name]
     extra = {"step": {"decode": "absorb_q + decode + out",
                       "append_decode": "cache_append (one token per sequence) + absorb_q + decode + out",
-                      "prefill": "cache_append (T tokens) + absorb_q + causal prefill + out"}[w.mode]}
+                      "prefill": "cache_append (T tokens) + absorb_q + causal prefill + out"}[w.mode]
+             + (" + out_proj (W_O)" if out_proj else "")}
     if "T" in case:
         extra["query_tokens"] = int(case["T"])
     return {"workload": name, "batch": int(case["seq_lens"].shape[0]), **extra,
@@ -258,6 +272,7 @@ def run_ours(args):
     prefill = mode == "prefill"
     pos = i32(case["append_pos"] if prefill else case["pos"])
     w_uk, w_uv = dev(case["w_uk"]), dev(case["w_uv"])
+    w_o = dev(case["w_o"]) if args.out_proj else None
     appending = mode in ("append_decode", "prefill")
     if appending:
         x, w_dkv, w_kr = dev(case["x"]), dev(case["w_dkv"]), dev(case["w_kr"])
@@ -267,11 +282,12 @@ def run_ours(args):
     o_lat = torch.empty((B, s.n_heads, s.d_latent), dtype=cfg.torch_dtype, device="cuda")
     lse = torch.empty((B, s.n_heads), dtype=torch.float32, device="cuda")
     o = torch.empty((B, s.n_heads * s.d_nope), dtype=cfg.torch_dtype, device="cuda")
+    out = torch.empty((B, s.d_model), dtype=cfg.torch_dtype, device="cuda") if args.out_proj else None
     ws = M.alloc_workspace(cfg)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step(qn=q_nope, qr=q_rope, xx=None, oo=o, ll=lse):
+    def step(qn=q_nope, qr=q_rope, xx=None, oo=o, ll=lse, ff=out):
         if appending:  # the same positions every step: the cache ends each step identical
             M.mla_cache_append(cfg, cache, x if xx is None else xx, w_dkv, w_kr, a_seq, a_pos, stream=stream)
         M.mla_absorb_q(cfg, qn, qr, pos, w_uk, q_cat=q_cat, stream=stream)
@@ -280,6 +296,8 @@ def run_ours(args):
         else:
             M.mla_decode(cfg, cache, q_cat, o_lat=o_lat, lse=ll, workspace=ws, stream=stream)
         M.mla_out(cfg, o_lat, w_uv, o=oo, stream=stream)
+        if args.out_proj:  # the layer output, out = o . W_O
+            M.mla_out_proj(cfg, oo, w_o, out=ff, stream=stream)
 
     warm = max(3, args.warmup)
     clocks = ClockSampler(local)
@@ -344,8 +362,13 @@ def run_ours(args):
     h_in, h_in_views = staging(ins, pinned=True)
     for hv, t in zip(h_in_views, ins):
         hv.copy_(t)
-    d_out, (e_o, e_lse) = staging([o, lse], pinned=False)
-    h_out, _ = staging([o, lse], pinned=True)
+    results = [out, lse] if args.out_proj else [o, lse]
+    d_out, e_res = staging(results, pinned=False)
+    h_out, _ = staging(results, pinned=True)
+    if args.out_proj:
+        e_o, e_lse, e_f = o, e_res[1], e_res[0]
+    else:
+        e_o, e_lse, e_f = e_res[0], e_res[1], out
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         dist.barrier()
@@ -354,7 +377,7 @@ def run_ours(args):
         flush.zero_()
         eev[i][0].record(stream)
         d_in.copy_(h_in, non_blocking=True)
-        step(e_in[0], e_in[1], e_in[2] if appending else None, e_o, e_lse)
+        step(e_in[0], e_in[1], e_in[2] if appending else None, e_o, e_lse, e_f)
         h_out.copy_(d_out, non_blocking=True)
         eev[i][1].record(stream)
     torch.cuda.synchronize()
@@ -386,7 +409,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": config_of(args.workload, case),
+        "config": config_of(args.workload, case, args.out_proj),
         "roofline": {"bound": "tensor" if tensor_bound else "hbm",
                      "achieved": alg_flops / k_mean_s / 1e12 if tensor_bound else achieved,
                      "peak": tflops if tensor_bound else hbm, "unit": "TFLOP/s" if tensor_bound else "GB/s",
@@ -411,7 +434,7 @@ def run_ours(args):
             t_cpu += cpu_oracle_sample(dict(case, seq_lens=case["seq_lens"][n_seq:],
                                              page_table=case["page_table"][n_seq:],
                                              q_nope=case["q_nope"][n_seq:], q_rope=case["q_rope"][n_seq:],
-                                             pos=case["pos"][n_seq:]), 1)
+                                             pos=case["pos"][n_seq:]), 1, args.out_proj)
             n_seq += 1
         line["cpu_baseline"] = {"value": n_seq / t_cpu, "unit": UNIT, "cores": cores(), "kind": "oracle",
                                 "sample": f"{n_seq} of {B} sequences (all 128 heads, 4096 cached tokens), "
@@ -430,6 +453,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_b16_l4096", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out-proj", action="store_true",
+                    help="add the output projection over the heads (W_O) to the timed step")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

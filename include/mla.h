@@ -37,7 +37,8 @@
  *     (griddepcontrol.launch_dependents; the library's own kernels do).  It waits for that
  *     kernel before reading what that kernel may write: q_cat and the cache rows in
  *     mla_decode / mla_prefill (written by mla_absorb_q and mla_cache_append), o_lat in
- *     mla_out, q_nope / q_rope / pos and x in mla_absorb_q and mla_cache_append.  The page
+ *     mla_out, o in mla_out_proj, q_nope / q_rope / pos and x in mla_absorb_q and
+ *     mla_cache_append.  The page
  *     table and lengths are read without the wait, so they must be produced
  *     by work that completes before the preceding kernel starts (ordinary kernels and copies
  *     do; MLA_TUNE_NO_PDL turns programmatic launch off).
@@ -190,6 +191,14 @@ MLA_API mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, in
  * n_tokens == 0 is a no-op. */
 MLA_API mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, void* o,
                    int32_t n_tokens, mla_stream_t stream);
+
+/* mla_out_proj - the final projection over the concatenated heads ([OPN] s.2 "out = O @ W_O";
+ * row block h of W_O belongs to head h):  out[n, :] = o[n, :] @ W_O
+ * o device [n_tokens, n_h*d_h] (what mla_out writes); w_o device [n_h*d_h, d_model];
+ * out device [n_tokens, d_model].  Rows of o and out must be multiples of 16 bytes
+ * (else MLA_ERR_UNSUPPORTED).  n_tokens == 0 is a no-op. */
+MLA_API mla_status mla_out_proj(const mla_config* cfg, const void* o, const void* w_o, void* out,
+                        int32_t n_tokens, mla_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_CUDA. */

@@ -17,7 +17,8 @@ from . import _lib
 from ._lib import MLAError, MLA_F32, MLA_BF16  # noqa: F401
 
 __all__ = ["MLAConfig", "PagedCache", "mla_cache_append", "mla_absorb_q", "mla_workspace_size",
-           "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_get_device_error", "mla_set_tuning",
+           "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_out_proj", "mla_get_device_error",
+           "mla_set_tuning",
            "mla_last_attention_path", "MLAError", "lib"]
 
 
@@ -163,6 +164,15 @@ def mla_out(cfg: MLAConfig, o_lat, w_uv, o=None, stream=None):
     st = lib().mla_out(ctypes.byref(cfg.c()), _ptr(o_lat), _ptr(w_uv), _ptr(o), n, _stream(stream))
     _lib.check(st, "mla_out")
     return o
+
+
+def mla_out_proj(cfg: MLAConfig, o, w_o, out=None, stream=None):
+    n = o.shape[0]
+    if out is None:
+        out = torch.empty((n, cfg.d_model), dtype=cfg.torch_dtype, device=o.device)
+    st = lib().mla_out_proj(ctypes.byref(cfg.c()), _ptr(o), _ptr(w_o), _ptr(out), n, _stream(stream))
+    _lib.check(st, "mla_out_proj")
+    return out
 
 
 def mla_get_device_error(stream=None) -> int:

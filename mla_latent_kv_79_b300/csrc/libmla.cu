@@ -47,7 +47,8 @@ static mla_status device_info(DeviceInfo** out) {
                 (const void*)simt_attention_kernel<bf16>, (const void*)simt_attention_kernel<float>,
                 (const void*)combine_kernel<bf16>, (const void*)combine_kernel<float>,
                 (const void*)tca::tc_attention_kernel, (const void*)tcg::tc_gemm_kernel<tcg::ABSORB>,
-                (const void*)tcg::tc_gemm_kernel<tcg::OUT>, (const void*)tcg::tc_gemm_kernel<tcg::APPEND>};
+                (const void*)tcg::tc_gemm_kernel<tcg::OUT>, (const void*)tcg::tc_gemm_kernel<tcg::APPEND>,
+                (const void*)tcg::tc_gemm_kernel<tcg::OPROJ>};
             for (const void* f : fns)
                 if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
@@ -447,6 +448,38 @@ mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, v
     g.C = o; g.ldc = (long long)n_h * d_h; g.c_batch = d_h;
     g.M = n_tokens; g.N = d_h; g.K = d_c;
     dim3 grid((d_h + 63) / 64, (n_tokens + 63) / 64, n_h);
+    if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    count_launches(1);
+    return launch_status();
+}
+
+mla_status mla_out_proj(const mla_config* cfg, const void* o, const void* w_o, void* out, int32_t n_tokens,
+                        mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!o || !w_o || !out || !aligned16(o) || !aligned16(w_o) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    const long long hd = (long long)cfg->n_heads * cfg->d_nope;
+    const int dm = cfg->d_model;
+    const size_t es = elem_size(cfg);
+    if (((size_t)hd * es) % 16 || ((size_t)dm * es) % 16 || hd > (1LL << 30)) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_oproj_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
+        st = tc_gemm_oproj(cfg, o, w_o, out, n_tokens,
+                           gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull), s);
+        if (st == MLA_OK) count_launches(1);
+        return st;
+    }
+    SimtGemmArgs g{};
+    g.A = o; g.lda = hd; g.a_batch = 0;
+    g.B = w_o; g.ldb_k = dm; g.ldb_n = 1; g.b_batch = 0;  // B(k, m) = W_O[k, m]
+    g.C = out; g.ldc = dm; g.c_batch = 0;
+    g.M = n_tokens; g.N = dm; g.K = (int)hd;
+    dim3 grid((dm + 63) / 64, (n_tokens + 63) / 64, 1);
     if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
     else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
     count_launches(1);

@@ -4,9 +4,10 @@
 //   out:    o[n, h*d_h + j] = sum_c W_UV[c, h*d_h + j] * o_lat[n, h, c]       (M = j, K = c)
 //   append: row[n, c] = sum_k [W_DKV | W_KR][k, c] * x[n, k], stored to the paged pool with
 //           RoPE(., pos[n]) on the last d_r columns                            (M = c, K = k)
+//   oproj:  out[n, m] = sum_k W_O[k, m] * o[n, k], k over n_h*d_h               (M = m, K = k)
 //
 // All are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
-// 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, W_DKV and W_KR, as the
+// 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, W_DKV, W_KR and W_O, as the
 // weights are stored) and up to 256 tokens as B (K-major).  Each CTA owns one m-tile of up to HPC heads for one n-tile:
 // warp 0 streams 64-wide K chunks of A and B through a ring that fills shared memory, warp 1
 // issues the MMAs into one TMEM accumulator per head, warps 2-5 drain D (one row per thread).
@@ -28,7 +29,8 @@ namespace tcg {
 
 constexpr int BM = 128, BK = 64, MAX_N = 256, HPC = 4, MAX_STAGES = 16;
 constexpr int MAX_KSPLIT = 8;                 // portable cluster size
-constexpr int SPLIT_STAGES = 4;               // ring depth of split-K CTAs (a few share an SM)
+constexpr int SPLIT_STAGES = 3;               // ring depth of split-K CTAs (several share an SM)
+constexpr int SPLIT_BELOW_CTAS = 148;         // fewer output tiles than SMs: split K
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int NTHREADS = 192;
 constexpr int SMEM_LIMIT = 232448;            // opt-in shared memory per CTA
@@ -60,7 +62,7 @@ inline int max_heads_per_cta(int n_pad) {
     return h < HPC ? h : HPC;
 }
 
-enum Mode { ABSORB = 0, OUT = 1, APPEND = 2 };
+enum Mode { ABSORB = 0, OUT = 1, APPEND = 2, OPROJ = 3 };
 
 struct GemmArgs {
     int mode;
@@ -197,7 +199,7 @@ __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, co
         const int n = n0 + nl;
         if (MODE == ABSORB) {
             out[((size_t)n * g.n_h + h0) * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
-        } else if (MODE == OUT) {
+        } else if (MODE == OUT || MODE == OPROJ) {  // OPROJ: n_h = 1, d_h = d_model
             out[(size_t)n * g.n_h * g.d_h + (size_t)h0 * g.d_h + mt * BM + tid] = __float2bfloat16_rn(v);
         } else if (!rope_tile) {
             if (rowoff[nl] >= 0) out[(size_t)rowoff[nl] * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
@@ -275,9 +277,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (MODE == ABSORB) {
                 // W_UK rows [mt*128, +128) x cols h*d_h + kc*64 .. +64 (K-major box 64 x 128)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + kc * BK, mt * BM, fb);
-            } else if (MODE == APPEND) {
-                // W_DKV (or, for the last tile, W_KR) rows k in [kc*64, +64) x output columns
-                // m .. m + 128 (MN-major, two boxes; columns past d_r read as zeros)
+            } else if (MODE == APPEND || MODE == OPROJ) {
+                // W_DKV / W_O (or, for the append's last tile, W_KR) rows k in [kc*64, +64) x
+                // output columns m .. m + 128 (MN-major, two boxes; columns past d_r read as zeros)
                 const CUtensorMap* t = rope_tile ? &tmA2 : &tmA;
                 const int m0 = rope_tile ? 0 : mt * BM;
                 ptx::tma_load_2d(st, t, m0, kc * BK, fb);
@@ -492,18 +494,20 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     if (g.n_tile == 0) g.n_tile = MAX_N;
     g.hpc = 1;
     if (t.hpc > 0) g.hpc = t.hpc < max_heads_per_cta(g.n_pad) ? t.hpc : max_heads_per_cta(g.n_pad);
-    // K split over a cluster: by default for APPEND with small token tiles (a decode step's few
-    // tokens leave only a handful of CTAs, each streaming K = d_model)
-    int ksp = t.ksplit > 0 ? t.ksplit : (g.mode == APPEND && g.n_tile <= 32 ? MAX_KSPLIT : 1);
+    // K split over a cluster by default when a deep K (d_model or n_h*d_h, streamed per CTA)
+    // would otherwise leave most SMs idle
+    const bool deep_k = g.mode == APPEND || g.mode == OPROJ;
+    const long long ctas = (long long)m_tiles * ((g.n_tokens + g.n_tile - 1) / g.n_tile);
+    int ksp = t.ksplit > 0 ? t.ksplit : (deep_k && ctas < SPLIT_BELOW_CTAS ? MAX_KSPLIT : 1);
     if (ksp > MAX_KSPLIT) ksp = MAX_KSPLIT;
     if (ksp > g.k_chunks) ksp = g.k_chunks;
     if (g.hpc != 1 || ksp < 1) ksp = 1;
     g.ksplit = ksp;
-    // ring depth: APPEND without a split streams K = d_model per CTA, as deep a ring as fits;
+    // ring depth: APPEND and OPROJ without a split stream a deep K per CTA, as deep a ring as fits;
     // never deeper than the chunks one CTA streams; with a split, deep enough to stage the
     // partial sums ([n_pad][128] fp32) where the ring was
     const int chunks = g.hpc * ((g.k_chunks + ksp - 1) / ksp), mx = max_stages(g.n_pad);
-    int S = ksp > 1 ? SPLIT_STAGES : g.mode == APPEND ? mx : stages_for(g.n_pad);
+    int S = ksp > 1 ? SPLIT_STAGES : deep_k ? mx : stages_for(g.n_pad);
     if (t.stages > 0) S = t.stages;
     if (S > chunks) S = chunks;
     if (ksp > 1) {
@@ -517,7 +521,10 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
     // one instantiation per mode: each launch fetches only its own code (cold after every L2
     // flush; instruction fetch stalls dominated this short kernel when the modes shared one)
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, GemmArgs) =
-        g.mode == ABSORB ? tc_gemm_kernel<ABSORB> : g.mode == OUT ? tc_gemm_kernel<OUT> : tc_gemm_kernel<APPEND>;
+        g.mode == ABSORB ? tc_gemm_kernel<ABSORB>
+        : g.mode == OUT  ? tc_gemm_kernel<OUT>
+        : g.mode == OPROJ ? tc_gemm_kernel<OPROJ>
+                          : tc_gemm_kernel<APPEND>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     cudaLaunchConfig_t lc = {};
@@ -596,6 +603,34 @@ inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void
         !tcg::encode_2d(&tb, o_lat, hc, (uint64_t)n, hc, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
     return tcg::launch(g, ta, tb, ta, c->d_nope / tcg::BM, c->n_heads, t, stream);
+}
+
+inline bool tc_gemm_oproj_supported(const mla_config* c, int n, int cc_major, int cc_minor) {
+    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 &&
+           ((long long)c->n_heads * c->d_nope) % 64 == 0 && c->d_model % 128 == 0;
+}
+
+// the output projection out = o . W_O on the tensor cores: one CTA per (128 output columns,
+// token tile).  W_O (n_h*d_h x d_model, 168 MB at DeepSeek-V2 sizes) is larger than L2, so up
+// to 256 tokens share one token tile and W_O is streamed once; K (n_h*d_h) is then split over
+// clusters of 8 CTAs to use the SMs
+inline mla_status tc_gemm_oproj(const mla_config* c, const void* o, const void* w_o, void* out, int n,
+                                const tcg::Tuning& t, cudaStream_t stream) {
+    tcg::GemmArgs g{};
+    g.mode = tcg::OPROJ;
+    g.n_tokens = n;
+    g.n_pad = tcg::n_pad_for(n);
+    g.n_tile = n <= tcg::MAX_N ? g.n_pad : tcg::MAX_N;
+    const uint64_t hd = (uint64_t)c->n_heads * c->d_nope;
+    g.k_chunks = (int)(hd / tcg::BK);
+    g.n_h = 1;
+    g.d_h = c->d_model;  // the epilogue's output row pitch
+    g.out = out;
+    CUtensorMap ta, tb;
+    if (!tcg::encode_2d(&ta, w_o, (uint64_t)c->d_model, hd, (uint64_t)c->d_model, 64) ||
+        !tcg::encode_2d(&tb, o, hd, (uint64_t)n, hd, (uint32_t)g.n_pad))
+        return MLA_ERR_CUDA;
+    return tcg::launch(g, ta, tb, ta, c->d_model / tcg::BM, 1, t, stream);
 }
 
 inline bool tc_gemm_append_supported(const mla_config* c, int n, int cc_major, int cc_minor) {

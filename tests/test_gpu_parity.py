@@ -162,11 +162,27 @@ def test_out_matches_oracle(path, dtype, shape, n):
     assert rel(host(out.t), ref) <= tol(dtype)[0]
 
 
+@pytest.mark.parametrize("dtype,shape,n", [("bf16", DS, 37), ("bf16", DS, 200), ("f32", W.TINY, 5)])
+def test_out_proj_matches_oracle(path, dtype, shape, n):
+    """The final projection over the concatenated heads, out = o . W_O, against the oracle's."""
+    r = np.random.default_rng(44)
+    o = W.quantise(W.normal(r, (n, shape.n_heads * shape.d_nope)), dtype)
+    w_o = W.weight(r, shape.n_heads * shape.d_nope, shape.d_model, dtype)
+    cfg = cfg_of(shape, dtype)
+    out = Guarded((n, shape.d_model), cfg.torch_dtype)
+    M.mla_out_proj(cfg, dev(o, dtype), dev(w_o, dtype), out=out.t)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    out.check()
+    assert rel(host(out.t), O.output_projection(f64(o, dtype), f64(w_o, dtype))) <= tol(dtype)[0]
+
+
 @pytest.mark.parametrize("ksplit,stages", [(1, 0), (2, 0), (3, 0), (8, 2)])
 def test_gemm_k_split_matches_oracle(ksplit, stages):
     """The tcgen05 GEMMs with K split over a cluster forced to uneven splits (W_UV's 8 K chunks
-    in 3 parts, d_model's 80 in 3 or 8), and with the split turned off (1) for a decode-sized
-    append: every mode's result is the oracle's whatever the split."""
+    in 3 parts, d_model's 80 and W_O's 256 in 3 or 8), and with the split turned off (1) for a
+    decode-sized append and output projection: every mode's result is the oracle's whatever the
+    split."""
     M.mla_set_tuning(_lib.MLA_TUNE_FORCE_SIMT, 0)
     old_k = M.mla_set_tuning(_lib.MLA_TUNE_GEMM_KSPLIT, ksplit)
     old_s = M.mla_set_tuning(_lib.MLA_TUNE_GEMM_STAGES, stages)
@@ -184,6 +200,11 @@ def test_gemm_k_split_matches_oracle(ksplit, stages):
         w_uv = W.weight(r, DS.d_latent, DS.n_heads * DS.d_nope, "bf16")
         o = Guarded((n, DS.n_heads * DS.d_nope), cfg.torch_dtype)
         M.mla_out(cfg, dev(o_lat), dev(w_uv), o=o.t)
+        # output projection over the heads
+        o_in = W.quantise(W.normal(r, (n, DS.n_heads * DS.d_nope)), "bf16")
+        w_o = W.weight(r, DS.n_heads * DS.d_nope, DS.d_model, "bf16")
+        op = Guarded((n, DS.d_model), cfg.torch_dtype)
+        M.mla_out_proj(cfg, dev(o_in), dev(w_o), out=op.t)
         # append: one token per sequence at ragged positions
         lens = r.integers(1, 200, size=n)
         pt, n_pages = W.make_page_table(r, [int(l) + 1 for l in lens], DS.page_size, 2, True)
@@ -197,6 +218,8 @@ def test_gemm_k_split_matches_oracle(ksplit, stages):
         assert_no_device_error()
         q_cat.check()
         o.check()
+        op.check()
+        assert rel(host(op.t), O.output_projection(f64(o_in), f64(w_o))) <= TOL_OUT_BF16
         ref = O.absorb_query(f64(case["q_nope"]), f64(case["q_rope"]), pos, f64(case["w_uk"]), DS.rope_base)
         got = host(q_cat.t)
         assert rel(got[..., :DS.d_latent], ref[..., :DS.d_latent]) <= TOL_OUT_BF16
@@ -440,7 +463,7 @@ def test_tiny_f32_chain_matches_unabsorbed_oracle(path):
     assert rel(out, ref_out) <= TOL_OUT_F32
 
 
-def test_bf16_chain_append_absorb_decode_out(path):
+def test_bf16_chain_append_absorb_decode_out_proj(path):
     lens = [100, 64, 1, 700]
     case = W.make_decode_case(DS, "bf16", lens, seed=71, append=True)
     cfg = cfg_of(DS, "bf16")
@@ -451,9 +474,10 @@ def test_bf16_chain_append_absorb_decode_out(path):
                            dev(case["w_uk"]))
     o_lat, lse = M.mla_decode(cfg, cache, q_cat)
     o = M.mla_out(cfg, o_lat, dev(case["w_uv"]))
+    out = M.mla_out_proj(cfg, o, dev(case["w_o"]))
     torch.cuda.synchronize()
     assert_no_device_error()
-    go, gl, gol = host(o), host(lse), host(o_lat)
+    go, gl, gol, gout = host(o), host(lse), host(o_lat), host(out)
     sc = O.default_scale(DS.d_nope, DS.d_rope)
     x = f64(case["x"])
     c_new, k_new = O.latent_kv(x, f64(case["w_dkv"]), f64(case["w_kr"]), case["append_pos"], DS.rope_base)
@@ -467,6 +491,8 @@ def test_bf16_chain_append_absorb_decode_out(path):
                                                 f64(case["w_uk"]), f64(case["w_uv"]), sc)
         assert rel(gol[b], rol) <= TOL_OUT_BF16, b
         assert rel(go[b], ro.reshape(-1)) <= TOL_OUT_BF16, b
+        # the whole layer output, the un-absorbed chain through W_O
+        assert rel(gout[b], O.output_projection(ro.reshape(1, -1), f64(case["w_o"]))[0]) <= TOL_OUT_BF16, b
         # the path stores q_cat and the appended cache row in bf16 before attention reads them
         q_cat = O.absorb_query(f64(case["q_nope"])[b:b + 1], f64(case["q_rope"])[b:b + 1],
                                case["pos"][b:b + 1], f64(case["w_uk"]), DS.rope_base)[0]
