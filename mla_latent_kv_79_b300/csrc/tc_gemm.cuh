@@ -194,8 +194,18 @@ __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, co
     bf16* out = reinterpret_cast<bf16*>(MODE == APPEND ? g.pool : g.out);
     for (int nl = t0; nl < t1; ++nl) {
         const uint32_t a = base + (uint32_t)(nl * BM + tid) * 4u;
+        // four ranks' loads in flight per add round; the sum is still in rank order
         float v = 0.f;
-        for (int r = 0; r < KS; ++r) v += ptx::ld_cluster_f32(ptx::mapa(a, (uint32_t)r));
+#pragma unroll 1
+        for (int r0 = 0; r0 < KS; r0 += 4) {
+            float part[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                part[r] = r0 + r < KS ? ptx::ld_cluster_f32(ptx::mapa(a, (uint32_t)(r0 + r))) : 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r0 + r < KS) v += part[r];
+        }
         const int n = n0 + nl;
         if (MODE == ABSORB) {
             out[((size_t)n * g.n_h + h0) * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
