@@ -1,4 +1,4 @@
-// tcgen05 GEMM for the per-head projections around the attention (sm_103a, bf16, fp32 acc).
+// tcgen05 GEMM for the projections around the attention (sm_103a, bf16, fp32 accumulation).
 //
 //   absorb: q_cat[n, h, c] = sum_j W_UK[c, h*d_h + j] * q_nope[n, h, j]      (M = c, K = j)
 //   out:    o[n, h*d_h + j] = sum_c W_UV[c, h*d_h + j] * o_lat[n, h, c]       (M = j, K = c)
@@ -8,16 +8,17 @@
 //
 // All are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
 // 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, W_DKV, W_KR and W_O, as the
-// weights are stored) and up to 256 tokens as B (K-major).  Each CTA owns one m-tile of up to HPC heads for one n-tile:
-// warp 0 streams 64-wide K chunks of A and B through a ring that fills shared memory, warp 1
-// issues the MMAs into one TMEM accumulator per head, warps 2-5 drain D (one row per thread).
-// With few tokens (decode) a CTA's whole weight slice is in flight at once.  The kernel is
-// launched as a programmatic dependent: the weights do not depend on the previous kernel, so
-// their loads are issued before the grid-dependency wait and only the token operand after it.
-// In ABSORB mode the CTAs also write the RoPE half of q_cat (RoPE(q_rope[n, h], pos[n]) into
-// columns [d_c, d_c + d_r)), spread over all CTAs of a token tile, with the epilogue warps,
-// which are idle while the weights stream.  Few tokens with a deep K (APPEND in a decode step)
-// split K over a cluster of CTAs that add their partial sums through distributed shared memory.
+// weights are stored) and up to 256 tokens as B (K-major).  Each CTA owns one m-tile of up to
+// HPC heads for one n-tile: warp 0 streams 64-wide K chunks of A and B through a ring that
+// fills shared memory, warp 1 issues the MMAs into one TMEM accumulator per head, warps 2-5
+// drain D (one row per thread).  With few tokens (decode) a CTA's whole weight slice is in
+// flight at once.  The kernel is launched as a programmatic dependent: the weights do not
+// depend on the previous kernel, so their loads are issued before the grid-dependency wait and
+// only the token operand after it.  In ABSORB mode the CTAs also write the RoPE half of q_cat
+// (RoPE(q_rope[n, h], pos[n]) into columns [d_c, d_c + d_r)), spread over all CTAs of a token
+// tile, with the epilogue warps, which are idle while the weights stream.  A deep K (APPEND's
+// d_model, OPROJ's n_h*d_h) over too few output tiles is split over a cluster of CTAs that add
+// their partial sums through distributed shared memory.  Each mode is its own instantiation.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -44,9 +45,9 @@ __host__ __device__ inline uint32_t tmem_cols(int n_pad) {
     while ((int)c < n_pad) c <<= 1;
     return c;
 }
-// Ring depth.  Few tokens: three stages, so that four CTAs share an SM (measured on B300: the
-// weight streams gain from more resident CTAs, not from a deeper ring per CTA).  Many tokens:
-// as deep as shared memory allows.
+// Ring depth.  Few tokens: at most three stages (and no more than the chunks a CTA streams), so
+// that several CTAs share an SM (measured on B300: the weight streams gain from more resident
+// CTAs, not from a deeper ring per CTA).  Many tokens: as deep as shared memory allows.
 inline int max_stages(int n_pad) {
     int s = (SMEM_LIMIT - 48 - 4 * MAX_N) / (stage_bytes(n_pad) + 16);
     return s < MAX_STAGES ? s : MAX_STAGES;
