@@ -1,0 +1,68 @@
+"""The benchmark's host-side helpers that feed the roofline object: algorithmic bytes and FLOPs
+of one attention launch, and the DRAM traffic read from a committed ncu summary, which must be
+dropped (null) as soon as the profiled kernel's own sources change."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import mla_workloads as W  # noqa: E402
+
+
+def test_decode_algorithmic_bytes_and_flops_match_the_hand_count():
+    # B=16 sequences of 4096 tokens, 128 heads, rows of 576 bf16, latent 512
+    case = {"shape": W.DEEPSEEK_V2, "seq_lens": np.full(16, 4096, dtype=np.int32)}
+    b, f = bench.workload_numbers(case)
+    per_seq = 4096 * 576 * 2 + 128 * 576 * 2 + 128 * (512 * 2 + 4)
+    assert b == 16 * per_seq == 79962112
+    assert f == 16 * 2 * 4096 * 128 * (576 + 512) == 18253611008
+
+
+def test_prefill_flops_count_the_causal_triangle():
+    T = 5
+    case = {"shape": W.DEEPSEEK_V2, "seq_lens": np.array([T], dtype=np.int32), "T": T}
+    b, f = bench.workload_numbers(case)
+    pairs = sum(i + 1 for i in range(T))  # query i sees tokens 0..i
+    assert f == 2 * 128 * (576 + 512) * pairs
+    assert b == T * 576 * 2 + T * (128 * 576 * 2 + 128 * (512 * 2 + 4))
+
+
+def test_source_digest_is_per_kernel():
+    a = bench.source_digest("tc_attention")
+    g = bench.source_digest("tc_gemm")
+    assert a != g and a != bench.source_digest()
+    for files in bench.KERNEL_SOURCES.values():
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, "mla_latent_kv_79_b300", "csrc", f)), f
+
+
+def _write_profile(d, digest, nbytes=12345):
+    p = d / "tc_attention_decode_b16_l4096.md"
+    p.write_text(f"# capture\n\n- dram_bytes_per_launch: {nbytes}\n- source_digest: {digest} (of some files)\n")
+
+
+def test_traffic_is_read_when_the_kernel_sources_match(tmp_path, monkeypatch):
+    _write_profile(tmp_path, bench.source_digest("tc_attention"))
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    assert bench.ncu_traffic("tc_attention", "decode_b16_l4096") == 12345
+
+
+def test_traffic_is_null_once_the_kernel_sources_changed(tmp_path, monkeypatch):
+    _write_profile(tmp_path, "0123456789abcdef")
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    assert bench.ncu_traffic("tc_attention", "decode_b16_l4096") is None
+    # and a missing summary is null too
+    assert bench.ncu_traffic("tc_attention", "decode_long_b4") is None
+
+
+@pytest.mark.parametrize("out_proj", [False, True])
+def test_config_names_the_step(out_proj):
+    case = {"shape": W.DEEPSEEK_V2, "seq_lens": np.full(16, 4096, dtype=np.int32)}
+    c = bench.config_of("decode_b16_l4096", case, out_proj)
+    assert c["workload"] == "decode_b16_l4096" and c["batch"] == 16 and c["seq_len"] == 4096
+    assert ("W_O" in c["step"]) == out_proj
