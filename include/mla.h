@@ -37,8 +37,8 @@
  *     (griddepcontrol.launch_dependents; the library's own kernels do).  It waits for that
  *     kernel before reading what that kernel may write: q_cat and the cache rows in
  *     mla_decode / mla_prefill (written by mla_absorb_q and mla_cache_append), o_lat in
- *     mla_out, o in mla_out_proj, q_nope / q_rope / pos and x in mla_absorb_q and
- *     mla_cache_append.  The page
+ *     mla_out, o in mla_out_proj, x in mla_query_proj, q_nope / q_rope / pos and x in
+ *     mla_absorb_q and mla_cache_append.  The page
  *     table and lengths are read without the wait, so they must be produced
  *     by work that completes before the preceding kernel starts (ordinary kernels and copies
  *     do; MLA_TUNE_NO_PDL turns programmatic launch off).
@@ -191,6 +191,16 @@ MLA_API mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, in
  * n_tokens == 0 is a no-op. */
 MLA_API mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, void* o,
                    int32_t n_tokens, mla_stream_t stream);
+
+/* mla_query_proj - the query side in its simplest form ([OPN] s.2 "Q = x @ W_Q", no query
+ * compression) plus the per-head RoPE query of [GLO]'s decoupled key:
+ *   q_nope[n] = x[n] @ W_Q   and   q_rope[n] = x[n] @ W_QR   (q_rope unrotated: mla_absorb_q
+ *   applies RoPE at the token's position)
+ * x device [n_tokens, d_model]; w_q device [d_model, n_h*d_h]; w_qr device [d_model, n_h*d_r];
+ * q_nope device [n_tokens, n_h, d_h]; q_rope device [n_tokens, n_h, d_r].  Rows must be
+ * multiples of 16 bytes (else MLA_ERR_UNSUPPORTED).  n_tokens == 0 is a no-op. */
+MLA_API mla_status mla_query_proj(const mla_config* cfg, const void* x, const void* w_q, const void* w_qr,
+                          void* q_nope, void* q_rope, int32_t n_tokens, mla_stream_t stream);
 
 /* mla_out_proj - the final projection over the concatenated heads ([OPN] s.2 "out = O @ W_O";
  * row block h of W_O belongs to head h):  out[n, :] = o[n, :] @ W_O

@@ -17,7 +17,8 @@ from . import _lib
 from ._lib import MLAError, MLA_F32, MLA_BF16  # noqa: F401
 
 __all__ = ["MLAConfig", "PagedCache", "mla_cache_append", "mla_absorb_q", "mla_workspace_size",
-           "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_out_proj", "mla_get_device_error",
+           "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_out_proj", "mla_query_proj",
+           "mla_get_device_error",
            "mla_set_tuning",
            "mla_last_attention_path", "MLAError", "lib"]
 
@@ -164,6 +165,18 @@ def mla_out(cfg: MLAConfig, o_lat, w_uv, o=None, stream=None):
     st = lib().mla_out(ctypes.byref(cfg.c()), _ptr(o_lat), _ptr(w_uv), _ptr(o), n, _stream(stream))
     _lib.check(st, "mla_out")
     return o
+
+
+def mla_query_proj(cfg: MLAConfig, x, w_q, w_qr, q_nope=None, q_rope=None, stream=None):
+    n = x.shape[0]
+    if q_nope is None:
+        q_nope = torch.empty((n, cfg.n_heads, cfg.d_nope), dtype=cfg.torch_dtype, device=x.device)
+    if q_rope is None:
+        q_rope = torch.empty((n, cfg.n_heads, cfg.d_rope), dtype=cfg.torch_dtype, device=x.device)
+    st = lib().mla_query_proj(ctypes.byref(cfg.c()), _ptr(x), _ptr(w_q), _ptr(w_qr), _ptr(q_nope), _ptr(q_rope), n,
+                              _stream(stream))
+    _lib.check(st, "mla_query_proj")
+    return q_nope, q_rope
 
 
 def mla_out_proj(cfg: MLAConfig, o, w_o, out=None, stream=None):

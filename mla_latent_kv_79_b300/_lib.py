@@ -49,6 +49,7 @@ SIGNATURES = {
     "mla_prefill": (_I, [_CFG, _CACHE, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_out": (_I, [_CFG, _P, _P, _P, _I, _P]),
     "mla_out_proj": (_I, [_CFG, _P, _P, _P, _I, _P]),
+    "mla_query_proj": (_I, [_CFG, _P, _P, _P, _P, _P, _I, _P]),
     "mla_get_device_error": (_I, [_P]),
     "mla_set_tuning": (_I, [_I, _I]),
     "mla_last_attention_path": (_I, []),

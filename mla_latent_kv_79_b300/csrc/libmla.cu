@@ -454,6 +454,9 @@ mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, v
     return launch_status();
 }
 
+static mla_status dense_projection(const mla_config* cfg, const DeviceInfo* dev, const void* in, const void* w,
+                                   void* out, long long K, long long M, int32_t n_tokens, cudaStream_t s);
+
 mla_status mla_out_proj(const mla_config* cfg, const void* o, const void* w_o, void* out, int32_t n_tokens,
                         mla_stream_t stream) {
     mla_status st = check_config(cfg);
@@ -468,22 +471,51 @@ mla_status mla_out_proj(const mla_config* cfg, const void* o, const void* w_o, v
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DeviceInfo* dev;
     if ((st = device_info(&dev)) != MLA_OK) return st;
-    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_oproj_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor)) {
-        st = tc_gemm_oproj(cfg, o, w_o, out, n_tokens,
-                           gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull), s);
+    return dense_projection(cfg, dev, o, w_o, out, hd, dm, n_tokens, s);
+}
+
+// out[n, :] = in[n, :] . W (W [K, M] row-major) on the tensor cores where they apply, else the
+// portable SIMT GEMM
+static mla_status dense_projection(const mla_config* cfg, const DeviceInfo* dev, const void* in, const void* w,
+                                   void* out, long long K, long long M, int32_t n_tokens, cudaStream_t s) {
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_dense_supported(cfg, K, M, n_tokens, dev->cc_major, dev->cc_minor)) {
+        const mla_status st = tc_gemm_dense(cfg, in, w, out, K, M, n_tokens,
+                                            gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull), s);
         if (st == MLA_OK) count_launches(1);
         return st;
     }
     SimtGemmArgs g{};
-    g.A = o; g.lda = hd; g.a_batch = 0;
-    g.B = w_o; g.ldb_k = dm; g.ldb_n = 1; g.b_batch = 0;  // B(k, m) = W_O[k, m]
-    g.C = out; g.ldc = dm; g.c_batch = 0;
-    g.M = n_tokens; g.N = dm; g.K = (int)hd;
-    dim3 grid((dm + 63) / 64, (n_tokens + 63) / 64, 1);
+    g.A = in; g.lda = K; g.a_batch = 0;
+    g.B = w; g.ldb_k = M; g.ldb_n = 1; g.b_batch = 0;  // B(k, m) = W[k, m]
+    g.C = out; g.ldc = M; g.c_batch = 0;
+    g.M = n_tokens; g.N = (int)M; g.K = (int)K;
+    dim3 grid((unsigned)((M + 63) / 64), (unsigned)((n_tokens + 63) / 64), 1);
     if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
     else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
     count_launches(1);
     return launch_status();
+}
+
+mla_status mla_query_proj(const mla_config* cfg, const void* x, const void* w_q, const void* w_qr, void* q_nope,
+                          void* q_rope, int32_t n_tokens, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!x || !w_q || !w_qr || !q_nope || !q_rope || !aligned16(x) || !aligned16(w_q) || !aligned16(w_qr) ||
+        !aligned16(q_nope) || !aligned16(q_rope))
+        return MLA_ERR_INVALID_ARG;
+    const long long hd = (long long)cfg->n_heads * cfg->d_nope, hr = (long long)cfg->n_heads * cfg->d_rope;
+    const int dm = cfg->d_model;
+    const size_t es = elem_size(cfg);
+    if (((size_t)hd * es) % 16 || ((size_t)hr * es) % 16 || ((size_t)dm * es) % 16 || hd > (1LL << 30) ||
+        hr > (1LL << 30))
+        return MLA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    if ((st = dense_projection(cfg, dev, x, w_q, q_nope, dm, hd, n_tokens, s)) != MLA_OK) return st;
+    return dense_projection(cfg, dev, x, w_qr, q_rope, dm, hr, n_tokens, s);
 }
 
 mla_status mla_get_device_error(mla_stream_t stream) {

@@ -616,32 +616,33 @@ inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void
     return tcg::launch(g, ta, tb, ta, c->d_nope / tcg::BM, c->n_heads, t, stream);
 }
 
-inline bool tc_gemm_oproj_supported(const mla_config* c, int n, int cc_major, int cc_minor) {
-    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 &&
-           ((long long)c->n_heads * c->d_nope) % 64 == 0 && c->d_model % 128 == 0;
+// a dense projection out[n, :] = in[n, :] . W with W [K, M] row-major (M contiguous), the
+// OPROJ mode: W as the MN-major A operand, K a multiple of 64, M of 128, bf16
+inline bool tc_gemm_dense_supported(const mla_config* c, long long K, long long M, int n, int cc_major,
+                                    int cc_minor) {
+    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 && K % 64 == 0 && M % 128 == 0 &&
+           K <= (1LL << 24) && M <= (1LL << 24);
 }
 
-// the output projection out = o . W_O on the tensor cores: one CTA per (128 output columns,
-// token tile).  W_O (n_h*d_h x d_model, 168 MB at DeepSeek-V2 sizes) is larger than L2, so up
-// to 256 tokens share one token tile and W_O is streamed once; K (n_h*d_h) is then split over
-// clusters of 8 CTAs to use the SMs
-inline mla_status tc_gemm_oproj(const mla_config* c, const void* o, const void* w_o, void* out, int n,
-                                const tcg::Tuning& t, cudaStream_t stream) {
+// One CTA per (128 output columns, token tile).  W (168 MB for W_O, W_Q at DeepSeek-V2 sizes)
+// can be larger than L2, so up to 256 tokens share one token tile and W is streamed once; K is
+// then split over clusters of 8 CTAs when the output tiles alone would leave SMs idle.
+inline mla_status tc_gemm_dense(const mla_config* c, const void* in, const void* w, void* out, long long K,
+                                long long M, int n, const tcg::Tuning& t, cudaStream_t stream) {
     tcg::GemmArgs g{};
     g.mode = tcg::OPROJ;
     g.n_tokens = n;
     g.n_pad = tcg::n_pad_for(n);
     g.n_tile = n <= tcg::MAX_N ? g.n_pad : tcg::MAX_N;
-    const uint64_t hd = (uint64_t)c->n_heads * c->d_nope;
-    g.k_chunks = (int)(hd / tcg::BK);
+    g.k_chunks = (int)(K / tcg::BK);
     g.n_h = 1;
-    g.d_h = c->d_model;  // the epilogue's output row pitch
+    g.d_h = (int)M;  // the epilogue's output row pitch
     g.out = out;
     CUtensorMap ta, tb;
-    if (!tcg::encode_2d(&ta, w_o, (uint64_t)c->d_model, hd, (uint64_t)c->d_model, 64) ||
-        !tcg::encode_2d(&tb, o, hd, (uint64_t)n, hd, (uint32_t)g.n_pad))
+    if (!tcg::encode_2d(&ta, w, (uint64_t)M, (uint64_t)K, (uint64_t)M, 64) ||
+        !tcg::encode_2d(&tb, in, (uint64_t)K, (uint64_t)n, (uint64_t)K, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
-    return tcg::launch(g, ta, tb, ta, c->d_model / tcg::BM, 1, t, stream);
+    return tcg::launch(g, ta, tb, ta, (int)(M / tcg::BM), 1, t, stream);
 }
 
 inline bool tc_gemm_append_supported(const mla_config* c, int n, int cc_major, int cc_minor) {

@@ -162,6 +162,33 @@ def test_out_matches_oracle(path, dtype, shape, n):
     assert rel(host(out.t), ref) <= tol(dtype)[0]
 
 
+@pytest.mark.parametrize("dtype,shape,n", [("bf16", DS, 37), ("f32", W.TINY, 5)])
+def test_query_proj_then_absorb_matches_oracle(path, dtype, shape, n):
+    """The query side, q_nope = x . W_Q and q_rope = x . W_QR (unrotated), then mla_absorb_q,
+    against the oracle's query projection (which rotates q_rope itself)."""
+    r = np.random.default_rng(45)
+    x = W.quantise(W.normal(r, (n, shape.d_model)), dtype)
+    w_q = W.weight(r, shape.d_model, shape.n_heads * shape.d_nope, dtype)
+    w_qr = W.weight(r, shape.d_model, shape.n_heads * shape.d_rope, dtype)
+    w_uk = W.weight(r, shape.d_latent, shape.n_heads * shape.d_nope, dtype)
+    pos = r.integers(0, 5000, size=n).astype(np.int32)
+    cfg = cfg_of(shape, dtype)
+    qn = Guarded((n, shape.n_heads, shape.d_nope), cfg.torch_dtype)
+    qr = Guarded((n, shape.n_heads, shape.d_rope), cfg.torch_dtype)
+    M.mla_query_proj(cfg, dev(x, dtype), dev(w_q, dtype), dev(w_qr, dtype), q_nope=qn.t, q_rope=qr.t)
+    q_cat = M.mla_absorb_q(cfg, qn.t, qr.t, i32(pos), dev(w_uk, dtype))
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    qn.check()
+    qr.check()
+    ref_qn, ref_qr = O.query_projection(f64(x, dtype), f64(w_q, dtype), f64(w_qr, dtype), pos, shape.n_heads,
+                                        shape.rope_base)
+    t_out = tol(dtype)[0]
+    assert rel(host(qn.t), ref_qn) <= t_out
+    # the RoPE half of q_cat is the oracle's rotated RoPE query (mla_absorb_q applies the rotation)
+    assert rel(host(q_cat)[..., shape.d_latent:], ref_qr) <= t_out
+
+
 @pytest.mark.parametrize("dtype,shape,n", [("bf16", DS, 37), ("bf16", DS, 200), ("f32", W.TINY, 5)])
 def test_out_proj_matches_oracle(path, dtype, shape, n):
     """The final projection over the concatenated heads, out = o . W_O, against the oracle's."""
