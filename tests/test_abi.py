@@ -27,7 +27,8 @@ def lib():
 def test_header_declares_the_hot_path():
     syms = declared_symbols()
     for name in ("mla_cache_append", "mla_absorb_q", "mla_decode", "mla_prefill", "mla_out",
-                 "mla_workspace_size", "mla_get_device_error", "mla_status_string"):
+                 "mla_out_proj", "mla_query_proj", "mla_workspace_size", "mla_get_device_error",
+                 "mla_status_string"):
         assert name in syms
 
 
@@ -90,12 +91,26 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.mla_prefill(ctypes.byref(cfg), ctypes.byref(cache), 5, 0, 1, 16, 16, 16, 16, 1 << 30, None) == 1
     assert lib.mla_prefill(ctypes.byref(cfg), ctypes.byref(cache), 0, 250, 10, 16, 16, 16, 16, 1 << 30, None) == 1
     assert lib.mla_decode(ctypes.byref(cfg), None, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mla_out_proj(ctypes.byref(cfg), None, 16, 16, 1, None) == 1
+    assert lib.mla_out_proj(ctypes.byref(cfg), 16, 24, 16, 1, None) == 1
+    assert lib.mla_query_proj(ctypes.byref(cfg), 16, 16, None, 16, 16, 1, None) == 1
+    assert lib.mla_query_proj(ctypes.byref(cfg), 16, 16, 16, 16, 40, 1, None) == 1
+    assert lib.mla_out_proj(ctypes.byref(cfg), 16, 16, 16, -1, None) == 1
 
 
 def test_zero_tokens_is_a_noop(lib):
     cfg = _cfg()
     assert lib.mla_absorb_q(ctypes.byref(cfg), None, None, None, None, None, 0, None) == 0
     assert lib.mla_out(ctypes.byref(cfg), None, None, None, 0, None) == 0
+    assert lib.mla_out_proj(ctypes.byref(cfg), None, None, None, 0, None) == 0
+    assert lib.mla_query_proj(ctypes.byref(cfg), None, None, None, None, None, 0, None) == 0
+
+
+def test_projection_rows_must_be_16_byte_multiples(lib):
+    # bf16 rows of d_model = 36 elements are 72 bytes: not a multiple of 16
+    cfg = _cfg(d_model=36)
+    assert lib.mla_out_proj(ctypes.byref(cfg), 16, 16, 16, 1, None) == 2
+    assert lib.mla_query_proj(ctypes.byref(cfg), 16, 16, 16, 16, 16, 1, None) == 2
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
