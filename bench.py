@@ -163,27 +163,73 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------ reference arm
 
-def cpu_oracle_sample(case, n_seq: int, out_proj: bool = False):
+def oracle_heads(case, budget_bytes: int = 4 << 30) -> int:
+    """Heads the CPU oracle times at once (a power of two dividing n_h): it restores K and V of
+    every head in float64, so long sequences would need tens of GB; the work is exactly linear
+    in heads."""
+    sh = case["shape"]
+    per_head = 2 * int(np.max(case["seq_lens"])) * sh.d_nope * 8
+    h = sh.n_heads
+    while h > 1 and (h * per_head > budget_bytes or sh.n_heads % h):
+        h //= 2
+    return h
+
+
+def cpu_oracle_sample(case, seqs, out_proj: bool = False, heads=None):
     """Time the float64 oracle (un-absorbed: restore K and V, softmax attention, W_UV folded
-    in by V, and W_O when out_proj) on the first n_seq sequences with all heads.  Returns
+    in by V, and W_O when out_proj) on sequences `seqs` with the first `heads` heads (all by
+    default); an append workload also runs the appended token's down-projection.  Returns
     seconds."""
     import oracle.mla_oracle as O
     s = case["shape"]
+    h = s.n_heads if heads is None else heads
     sc = O.default_scale(s.d_nope, s.d_rope)
     pool = case["pool"]
     f = lambda a: W.to_f64(a, case["dtype"])  # noqa: E731
-    w_uk, w_uv = f(case["w_uk"]), f(case["w_uv"])
-    w_o = f(case["w_o"]) if out_proj else None
+    w_uk, w_uv = f(case["w_uk"][:, :h * s.d_nope]), f(case["w_uv"][:, :h * s.d_nope])
+    w_o = f(case["w_o"][:h * s.d_nope]) if out_proj else None
+    appending = "x" in case and "append_pos" in case
+    if appending:
+        w_dkv, w_kr = f(case["w_dkv"]), f(case["w_kr"])
     t0 = time.perf_counter()
-    for b in range(n_seq):
+    for b in seqs:
+        if appending:
+            O.latent_kv(f(case["x"][b:b + 1]), w_dkv, w_kr, case["append_pos"][b:b + 1], s.rope_base)
         L = int(case["seq_lens"][b])
         rows = W.to_f64(W.gather_rows(pool, case["page_table"][b], L), case["dtype"])
-        q_r = O.rope_rotate(f(case["q_rope"][b]), case["pos"][b], s.rope_base)
-        o = O.attention_unabsorbed(f(case["q_nope"][b]), q_r, rows[:, :s.d_latent], rows[:, s.d_latent:],
+        q_r = O.rope_rotate(f(case["q_rope"][b][:h]), case["pos"][b], s.rope_base)
+        o = O.attention_unabsorbed(f(case["q_nope"][b][:h]), q_r, rows[:, :s.d_latent], rows[:, s.d_latent:],
                                    w_uk, w_uv, sc)[0]
         if out_proj:
             O.output_projection(o.reshape(1, -1), w_o)
     return time.perf_counter() - t0
+
+
+def oracle_sample_text(case, n_seq: int, n_all: int, heads: int, per_step: bool = False) -> str:
+    sh = case["shape"]
+    lens = case["seq_lens"][:n_seq]
+    toks = f"{int(lens[0])} cached tokens" if lens.min() == lens.max() else \
+        f"{int(lens.min())}-{int(lens.max())} cached tokens"
+    who = "one sequence per step" if per_step else f"{n_seq} of {n_all} sequences"
+    hs = f"all {sh.n_heads} heads" if heads == sh.n_heads else \
+        f"{heads} of {sh.n_heads} heads, time scaled by {sh.n_heads // heads} (the work is linear in heads)"
+    return f"{who} ({hs}, {toks}), un-absorbed float64 oracle"
+
+
+def cpu_baseline(case, out_proj: bool = False, budget_s: float = 10.0):
+    """The oracle timed on the host cores over a bounded sample of the workload: whole
+    sequences in order until about budget_s of oracle time, all heads unless the float64
+    restore would not fit (then a head subset, scaled up linearly)."""
+    sh = case["shape"]
+    B = int(case["seq_lens"].shape[0])
+    heads = oracle_heads(case)
+    n_seq, t_cpu = 0, 0.0
+    while n_seq < B and (n_seq == 0 or t_cpu < budget_s):
+        t_cpu += cpu_oracle_sample(case, [n_seq], out_proj, heads)
+        n_seq += 1
+    t_cpu *= sh.n_heads / heads
+    return {"value": n_seq / t_cpu, "unit": UNIT, "cores": cores(), "kind": "oracle",
+            "sample": oracle_sample_text(case, n_seq, B, heads)}
 
 
 def cores():
@@ -202,9 +248,11 @@ def run_reference(args):
               flush=True)
         return 0
     case = W.make_workload(args.workload)
+    heads = oracle_heads(case)
     for _ in range(max(0, args.warmup)):
-        cpu_oracle_sample(case, 1, args.out_proj)
-    ts = [cpu_oracle_sample(case, 1, args.out_proj) for _ in range(args.steps)]
+        cpu_oracle_sample(case, [0], args.out_proj, heads)
+    ts = [cpu_oracle_sample(case, [0], args.out_proj, heads) * (case["shape"].n_heads / heads)
+          for _ in range(args.steps)]
     t = sum(ts)
     value = args.steps / t
     line = {
@@ -213,8 +261,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(args.workload, case, args.out_proj),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                         "sample": "one sequence (4096 cached tokens, all 128 heads) per step, "
-                                   "un-absorbed float64 oracle"},
+                         "sample": oracle_sample_text(case, 1, 1, heads, per_step=True)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -427,18 +474,8 @@ def run_ours(args):
         "cpu_baseline": None,
         "step_us_median": 1e3 * statistics.median(step_ms),
     }
-    if not args.no_cpu_baseline and not appending:
-        n_seq = 0
-        t_cpu = 0.0
-        while n_seq < B and t_cpu < 10.0:
-            t_cpu += cpu_oracle_sample(dict(case, seq_lens=case["seq_lens"][n_seq:],
-                                             page_table=case["page_table"][n_seq:],
-                                             q_nope=case["q_nope"][n_seq:], q_rope=case["q_rope"][n_seq:],
-                                             pos=case["pos"][n_seq:]), 1, args.out_proj)
-            n_seq += 1
-        line["cpu_baseline"] = {"value": n_seq / t_cpu, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                                "sample": f"{n_seq} of {B} sequences (all 128 heads, 4096 cached tokens), "
-                                          "un-absorbed float64 oracle"}
+    if not args.no_cpu_baseline and not prefill:
+        line["cpu_baseline"] = cpu_baseline(case, args.out_proj)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

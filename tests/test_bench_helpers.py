@@ -66,3 +66,36 @@ def test_config_names_the_step(out_proj):
     c = bench.config_of("decode_b16_l4096", case, out_proj)
     assert c["workload"] == "decode_b16_l4096" and c["batch"] == 16 and c["seq_len"] == 4096
     assert ("W_O" in c["step"]) == out_proj
+
+
+def test_oracle_heads_keep_all_heads_unless_the_float64_restore_would_not_fit():
+    def heads(lens):
+        return bench.oracle_heads({"shape": W.DEEPSEEK_V2, "seq_lens": np.array(lens)})
+    assert heads([4096] * 16) == 128
+    assert heads([256, 8192]) == 128
+    h = heads([32768, 131072])
+    assert h < 128 and 128 % h == 0 and h * 2 * 131072 * 128 * 8 <= 4 << 30
+
+
+def test_oracle_sample_text_states_the_subset():
+    case = {"shape": W.DEEPSEEK_V2, "seq_lens": np.array([300, 500, 700])}
+    t = bench.oracle_sample_text(case, 2, 3, 16)
+    assert "2 of 3 sequences" in t and "16 of 128 heads" in t and "scaled by 8" in t and "300-500" in t
+    assert "all 128 heads" in bench.oracle_sample_text(case, 1, 3, 128)
+
+
+@pytest.mark.parametrize("append", [False, True])
+def test_cpu_oracle_sample_runs_on_a_head_subset(append):
+    case = W.make_decode_case(W.TINY, "f32", [10, 70], seed=3, append=append)
+    t_all = bench.cpu_oracle_sample(case, [0, 1], out_proj=True)
+    t_two = bench.cpu_oracle_sample(case, [1], out_proj=False, heads=2)
+    assert t_all > 0 and t_two > 0
+
+
+def test_cpu_baseline_line_is_bounded_and_described():
+    case = W.make_decode_case(W.TINY, "f32", [10, 70, 30], seed=4)
+    line = bench.cpu_baseline(case, out_proj=False, budget_s=0.0)  # stops after one sequence
+    assert line["kind"] == "oracle" and line["unit"] == bench.UNIT and line["value"] > 0
+    assert line["cores"] >= 1 and "1 of 3 sequences" in line["sample"]
+    full = bench.cpu_baseline(case, out_proj=True)
+    assert "3 of 3 sequences" in full["sample"] and "all 4 heads" in full["sample"]
