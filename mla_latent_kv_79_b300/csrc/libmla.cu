@@ -20,7 +20,7 @@ namespace mla {
 
 // ----------------------------------------------------------------------------- device info
 struct DeviceInfo {
-    bool ready = false;
+    std::atomic<bool> ready{false};  // published after the fields below are filled in
     int sms = 0, smem_optin = 0, cc_major = 0, cc_minor = 0;
 };
 static DeviceInfo g_dev[64];
@@ -30,9 +30,9 @@ static mla_status device_info(DeviceInfo** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
     DeviceInfo& d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_dev_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -53,7 +53,7 @@ static mla_status device_info(DeviceInfo** out) {
                 if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                     return MLA_ERR_CUDA;
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     *out = &d;
