@@ -7,7 +7,7 @@ import torch
 import mla_workloads as W
 from mla_latent_kv_79_b300 import MLAConfig, PagedCache
 
-# Tolerances (the benchmark spec): relative max-abs error on outputs, absolute on log-sum-exp.
+# Tolerances: relative max-abs error on outputs, absolute on log-sum-exp.
 TOL_OUT_BF16 = 2e-2
 TOL_LSE_BF16 = 1e-3
 # fp32 path: fp32 accumulation over at most a few thousand terms.
