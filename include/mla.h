@@ -67,7 +67,7 @@ typedef struct CUstream_st* mla_stream_t; /* a cudaStream_t */
 typedef enum {
     MLA_OK = 0,
     MLA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size or dimension          */
-    MLA_ERR_UNSUPPORTED = 2,    /* dimensions this build does not handle                    */
+    MLA_ERR_UNSUPPORTED = 2,    /* dimensions the library does not handle                   */
     MLA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed                     */
     MLA_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query returned */
     MLA_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait ran out (device error word)   */
