@@ -8,7 +8,6 @@ allocated here with torch (the library itself never allocates).
 from __future__ import annotations
 
 import ctypes
-import math
 from dataclasses import dataclass
 
 import torch
@@ -49,10 +48,6 @@ class MLAConfig:
     @property
     def torch_dtype(self):
         return _TORCH_DTYPE[self.dtype]
-
-    @property
-    def scale(self) -> float:
-        return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.d_nope + self.d_rope)
 
     def c(self) -> _lib.MlaConfig:
         return _lib.MlaConfig(self.n_heads, self.d_nope, self.d_rope, self.d_latent, self.d_model,

@@ -16,8 +16,6 @@ typedef __nv_bfloat16 bf16;
 
 // Per-device error word (first error wins).  Read and cleared by mla_get_device_error().
 __device__ int g_device_error = 0;
-// Bounded-wait limit for spin loops in nanoseconds (set from the host before launches).
-__device__ unsigned long long g_wait_limit_ns = 2000000000ull;
 
 __device__ __forceinline__ void set_device_error(int code) { atomicCAS(&g_device_error, 0, code); }
 

@@ -166,7 +166,10 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
 // loads with an online max, i.e. one memory round trip per batch.  The schedule arithmetic
 // reads only seq_lens, which the attention kernel does not write, so it runs before the
 // grid-dependency wait: launched as a programmatic dependent, it overlaps the attention
-// kernel's tail.
+// kernel's tail.  Every thread then waits for the attention grid before it stores anything or
+// leaves: o_lat and lse may still be read by an earlier kernel of the stream (the previous
+// step's output projection) until then, and the kernel after this one (which waits only for
+// this grid) must find the attention kernel's direct outputs complete.
 constexpr int COMBINE_THREADS = 256;
 constexpr int COMBINE_BATCH = 8;
 
@@ -229,6 +232,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
         sbase = (int)(2 * u_lo);
         first_adj = pq == u_lo * per ? 0 : 1;
     }
+    grid_dependency_wait();  // the attention grid is complete and its writes are visible
     if (np > 0 && ns == 1) return;  // written directly by the attention kernel
 
     const int e = blockIdx.y * blockDim.x + threadIdx.x;
@@ -240,7 +244,6 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(AttnArgs a) {
         if (grp == 0) a.lse[(long long)q * n_h + h] = -INFINITY;
         return;
     }
-    grid_dependency_wait();  // partials of the attention kernel are complete and visible
 
     float mx = -INFINITY, wsum = 0.f;
     float acc[V];

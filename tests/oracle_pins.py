@@ -198,6 +198,26 @@ def pin_attention_closed_forms(O):
     assert np.allclose(lse, math.log(math.exp(3.0) + 1.0), atol=1e-14)
 
 
+def pin_default_scale(O):
+    """The score scale 1/sqrt(d_h + d_r): the score is a dot product over the d_h nope and the
+    d_r RoPE dimensions (the decoupled key of the glossary), so the operator notes' division
+    by sqrt(d) of the dot product's width takes d = d_h + d_r."""
+    assert abs(O.default_scale(128, 64) - 1.0 / math.sqrt(192.0)) < 1e-17
+    assert abs(O.default_scale(16, 8) - 1.0 / math.sqrt(24.0)) < 1e-17
+    # tiny case: raw dot products 3*sqrt(d_h + d_r) and 0 are scaled to scores 3 and 0, so the
+    # first token's weight is 1 / (1 + e^-3) and lse = ln(e^3 + 1)
+    d_h, d_r, d_c = 16, 8, 4
+    rows = np.zeros((2, d_c + d_r))
+    rows[0, 0] = 1.0
+    rows[1, 1] = 1.0
+    q = np.zeros((1, d_c + d_r))
+    q[0, 0] = 3.0 * math.sqrt(d_h + d_r)
+    o_lat, lse = O.attention_latent(q, rows, d_c, O.default_scale(d_h, d_r))
+    p0 = 1.0 / (1.0 + math.exp(-3.0))
+    assert abs(o_lat[0, 0] - p0) < 1e-14 and abs(o_lat[0, 1] - (1.0 - p0)) < 1e-14
+    assert abs(lse[0] - math.log(math.exp(3.0) + 1.0)) < 1e-14
+
+
 def pin_softmax_properties(O):
     r = np.random.default_rng(16)
     s = r.standard_normal((4, 9)) * 5

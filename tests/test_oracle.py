@@ -130,6 +130,10 @@ def _mha_numbers_single(n_h, d_h):
     return n_h * d_h
 
 
+def _scale_sqrt_dh(d_nope, d_rope):
+    return 1.0 / math.sqrt(d_nope)
+
+
 def _gather_wrong_slot(pool, pt_row, length):
     pool = np.asarray(pool)
     ps = pool.shape[1]
@@ -152,6 +156,7 @@ MUTANTS = {
     "out_projection_transposed": dict(output_projection=_out_proj_transposed),
     "mha_count_drops_v": dict(mha_numbers_per_token=_mha_numbers_single),
     "paged_gather_wrong_slot": dict(sequence_rows=_gather_wrong_slot),
+    "default_scale_sqrt_dh": dict(default_scale=_scale_sqrt_dh),
 }
 
 

@@ -1,6 +1,6 @@
 """GPU tests of mla_decode_static, the decode entry point that allocates nothing (its split
 partials live in a fixed device array of the library).  Through the C ABI it must give
-mla_decode's results on the same inputs, on two calls in a row, without the device's free
+mla_decode's results on the same inputs (and the oracle's), on two calls in a row, without the device's free
 memory moving after the first call's set-up, and must reject a configuration whose scratch exceeds the array.
 
 The file is named to be collected last: it has to pass both after every other GPU test and
@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import mla_workloads as W
+import oracle.mla_oracle as O
 import mla_latent_kv_79_b300 as M
 from mla_latent_kv_79_b300 import _lib
 
@@ -32,6 +33,20 @@ def _compare(o, lse, o_ref, lse_ref):
             continue
         assert rel(go[b], ro[b]) <= TOL_OUT_BF16, b
         assert np.max(np.abs(gl[b] - rl[b])) <= TOL_LSE_BF16, b
+
+
+def _compare_oracle(case, o, lse):
+    """The static entry point's outputs against the CPU oracle itself."""
+    go, gl = host(o), host(lse)
+    sc = O.default_scale(DS.d_nope, DS.d_rope)
+    pool = W.to_f64(case["pool"], "bf16")
+    q = W.to_f64(case["q_cat"], "bf16")
+    for b, L in enumerate(LENS):
+        if L == 0:
+            continue
+        ro, rl = O.attention_latent(q[b], O.sequence_rows(pool, case["page_table"][b], L), DS.d_latent, sc)
+        assert rel(go[b], ro) <= TOL_OUT_BF16, b
+        assert np.max(np.abs(gl[b] - rl)) <= TOL_LSE_BF16, b
 
 
 @pytest.mark.parametrize("path", ["auto", "simt"])
@@ -63,6 +78,8 @@ def test_static_decode_matches_decode_twice(path):
                 assert torch.cuda.mem_get_info()[0] == free_before, f"call {i} moved free memory"
             assert M.mla_get_device_error() == 0
             _compare(o, lse, o_ref, lse_ref)
+            if i == 2:
+                _compare_oracle(case, o, lse)
     finally:
         M.mla_set_tuning(_lib.MLA_TUNE_FORCE_SIMT, old)
 
