@@ -98,7 +98,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     unsigned long long t0 = 0;
     for (uint32_t i = 0;; ++i) {
         if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
+        if (i & 1u) {  // every second failed poll (try_wait itself may suspend the thread)
             if (!w.ignore_abort && *w.abort) return false;
             const unsigned long long t = globaltimer_ns();
             if (t0 == 0) t0 = t;
@@ -118,7 +118,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     for (uint32_t i = 0;; ++i) {
         const bool ok = cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
-        if ((i & 63u) == 63u) {
+        if (i & 1u) {  // every second failed poll (try_wait itself may suspend the thread)
             int stop = 0;
             if (lane == 0) {
                 if (*w.abort) stop = 1;
@@ -231,9 +231,12 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
             ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
         }
     }
+    // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
+    // whatever the configured limit (which may be microseconds when a caller tests timeouts)
     ptx::tc_commit(bar_addr(base, B_DONE));
     WaitCtl w2 = wc;
     w2.ignore_abort = true;
+    w2.limit_ns = 20000000ull;
     wait_bar(bar_addr(base, B_DONE), 0, w2);
 }
 
@@ -372,9 +375,12 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
         }
         ++segn;
     }
+    // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
+    // whatever the configured limit (which may be microseconds when a caller tests timeouts)
     ptx::tc_commit(bar_addr(base, B_DONE));
     WaitCtl w2 = wc;
     w2.ignore_abort = true;
+    w2.limit_ns = 20000000ull;
     wait_bar(bar_addr(base, B_DONE), 0, w2);
 }
 

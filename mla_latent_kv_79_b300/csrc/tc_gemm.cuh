@@ -101,7 +101,7 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned lo
     unsigned long long t0 = 0;
     for (uint32_t i = 0;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u) {
+        if (i & 1u) {  // every second failed poll (try_wait itself may suspend the thread)
             const unsigned long long t = globaltimer_ns();
             if (t0 == 0) t0 = t;
             else if (t - t0 > limit) {
@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         grid_dependency_wait();
         for (int c = 0; c < pre; ++c) load_b(c, base + c * SB, bar_full + 8 * c);
+        int issued = pre;
         for (int c = pre; c < total; ++c) {
             const int s = c % S;
             if (!gwait(bar_empty + 8 * s, ((c / S) & 1u) ^ 1u, g.wait_ns)) break;
@@ -322,7 +323,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::mbar_arrive_expect_tx(fb, bytes);
             load_a(c, st, fb);
             load_b(c, st, fb);
+            issued = c + 1;
         }
+        // the last ring's worth of loads has landed before the CTA may leave (the consumer may have
+        // stopped early on a timeout); a fixed 20 ms bound
+        for (int c = issued > S ? issued - S : 0; c < issued; ++c) gwait(bar_full + 8 * (c % S), (c / S) & 1u, 20000000ull);
     } else if (warp == 1 && lane == 0) {
         const uint32_t idesc = ptx::idesc_bf16(BM, g.n_pad, a_mn, false);
         for (int c = 0; c < total; ++c) {
@@ -462,6 +467,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         ptx::cluster_sync();  // the peers have finished reading this CTA's shared memory
     }
+    // every MMA issued completes before TMEM is freed (the epilogue's own wait may have run out):
+    // the issuing thread waits for its final commit with a fixed 20 ms bound
+    if (warp == 1 && lane == 0) gwait(bar_done, 0, 20000000ull);
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
