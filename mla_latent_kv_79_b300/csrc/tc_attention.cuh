@@ -29,9 +29,10 @@
 // are in flight together.  The softmax warps (idle at a segment start) move their rows into
 // TMEM with tcgen05.st, so the tensor pipe is not held up by the copy.
 //
-// Roles (192 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
+// Roles (224 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
 // (one TMEM lane quarter each, one head per thread) softmax in the score CTA, rescale and
-// drain in the value CTA.  Every wait is bounded.
+// drain in the value CTA; warp 6 of the value CTA hands P buffers back to the score CTA as
+// their PVs complete.  Every wait is bounded.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -76,7 +77,7 @@ constexpr int OFF_RED = OFF_MISC + 16;            // schedule scratch (SCHED_SCR
 constexpr int SMEM_BYTES = OFF_RED + SCHED_SCRATCH * 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr int TM_Q = 0, TM_S = 288, TM_O = 0;
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;
 constexpr float TAU = 8.0f;  // log2 units
 constexpr float LN2 = 0.6931471805599453f;
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 64, false, false);
@@ -371,7 +372,6 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
             }
             ptx::tc_commit(bar_addr(base, B_PVDONE + pb));
             ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
-            ptx::tc_commit_mc(bar_addr(base, B_PEMPTY + pb), (uint16_t)0x1);
         }
         ++segn;
     }
@@ -488,6 +488,22 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
     }
 }
 
+// Value CTA, warp 6: as soon as the PV of page g has completed (its P buffer is read), tell the
+// score CTA that the buffer may be refilled.  A warp of its own, so that the signal waits for
+// nothing but that PV.
+__device__ __forceinline__ void value_release(const AttnArgs& a, UnitCursor c, uint32_t base, int lane,
+                                              const WaitCtl& wc) {
+    const uint32_t pempty_r = ptx::mapa(bar_addr(base, B_PEMPTY), 0);  // the score CTA's barriers
+    uint32_t g = 0;
+    Segment sg;
+    while (c.next(a.qs, &sg)) {
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
+            if (!warp_wait(bar_addr(base, B_PVDONE + (g & 1u)), (g >> 1) & 1u, wc, false, lane)) return;
+            if (lane == 0) ptx::mbar_arrive_remote(pempty_r + 8u * (g & 1u));
+        }
+    }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     tc_attention_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmq,
                         const TcArgs args) {
@@ -559,6 +575,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (rank == 0) score_mma(a, cur, base, tmem, wc);
             else value_mma(a, cur, base, tmem, wc);
         }
+    } else if (warp == 6) {
+        if (rank == 1) value_release(a, cur, base, lane, wc);
     } else if (rank == 0) {
         score_softmax(args, cur, base, tmem, peer, warp, lane, wc);
     } else {

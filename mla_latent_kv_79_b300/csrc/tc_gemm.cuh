@@ -182,6 +182,20 @@ __device__ __forceinline__ void absorb_rope(const GemmArgs& g, int n0, int tid) 
     }
 }
 
+// The 32 lanes of a warp hold one token's values of 32 consecutive latent columns (lane l:
+// column c0 + l).  Each group of 8 lanes packs its values to bf16 (round to nearest even, as a
+// single conversion would) and its first lane stores them as one 16-byte store at dst, its own
+// column's address (8-column aligned).  All lanes take part in the shuffles; `store` gates the
+// write (warp-uniform).
+__device__ __forceinline__ void store_cols8(bf16* dst, float v, int lane, bool store) {
+    const float nb = __shfl_down_sync(0xffffffffu, v, 1);
+    const uint32_t pair = ptx::pack_bf16(v, nb);  // meaningful in even lanes
+    const uint32_t p1 = __shfl_down_sync(0xffffffffu, pair, 2);
+    const uint32_t p2 = __shfl_down_sync(0xffffffffu, pair, 4);
+    const uint32_t p3 = __shfl_down_sync(0xffffffffu, pair, 6);
+    if (store && (lane & 7) == 0) *reinterpret_cast<uint4*>(dst) = make_uint4(pair, p1, p2, p3);
+}
+
 // Split K: the CTA of cluster rank ks adds the partial sums of all ksplit CTAs (in rank order,
 // so the result does not depend on timing) for its slice of the tile's tokens and stores them
 // as the mode's epilogue would.  Partials sit at the start of each CTA's shared memory as
@@ -213,7 +227,9 @@ __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, co
         } else if (MODE == OUT || MODE == OPROJ) {  // OPROJ: n_h = 1, d_h = d_model
             out[(size_t)n * g.n_h * g.d_h + (size_t)h0 * g.d_h + mt * BM + tid] = __float2bfloat16_rn(v);
         } else if (!rope_tile) {
-            if (rowoff[nl] >= 0) out[(size_t)rowoff[nl] * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
+            // latent columns: 16-byte stores of 8 columns (the row offset is per token, warp-uniform)
+            const int ro = rowoff[nl];
+            store_cols8(out + (size_t)(ro < 0 ? 0 : ro) * g.width + mt * BM + tid, v, tid & 31, ro >= 0);
         } else {
             // the pair (2i, 2i+1) sits in lanes tid, tid + 1 of one warp
             const float w = __shfl_xor_sync(0xffffffffu, v, 1);
@@ -396,7 +412,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bf16* pool = reinterpret_cast<bf16*>(g.pool);
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
             if (!rope_tile) {
-                // latent columns: per token, the 128 threads write 128 consecutive values
+                // latent columns: per token, the 128 threads hold 128 consecutive values, stored
+                // 8 columns per 16-byte store
                 const int c = mt * BM + row;
                 for (int c0 = 0; c0 < g.n_pad; c0 += 32) {
                     uint32_t r[32];
@@ -404,8 +421,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ptx::tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        if (c0 + i < n_here && rowoff[c0 + i] >= 0)
-                            pool[(size_t)rowoff[c0 + i] * g.width + c] = __float2bfloat16_rn(__uint_as_float(r[i]));
+                        if (c0 + i >= n_here) break;  // warp-uniform
+                        const int ro = rowoff[c0 + i];
+                        store_cols8(pool + (size_t)(ro < 0 ? 0 : ro) * g.width + c, __uint_as_float(r[i]), lane, ro >= 0);
                     }
                 }
             } else {
