@@ -16,6 +16,9 @@ already widened).  Citations name the page and its section:
          output projections; the MHA/GQA/MLA comparison table.
   [RMJ]  "Multi-Head Latent Attention and the Compression of the KV Cache" (rmj-insight
          dispatch): associativity lets the up-projection be absorbed into the query.
+  [IPM]  "Multi-Head Latent Attention (MLA) Explained: What DeepSeek's Architecture Means
+         for AI Inference Costs" (institutepm knowledge hub), section "Which Models Use MLA
+         and What Is Next": MXFP4 quantisation of the KV cache.
 
 Readings taken where the pages are silent (each is listed with its reason in the design
 notes of the repository):
@@ -30,6 +33,8 @@ Pins for every function live in tests/test_oracle.py (closed forms, brute-force 
 tiny inputs, the pages' cache-size integers, associativity between the two forms).
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -251,3 +256,151 @@ def sequence_rows(pool, page_table_row, length: int):
 
 def default_scale(d_nope: int, d_rope: int) -> float:
     return 1.0 / np.sqrt(F64(d_nope + d_rope))
+
+
+# ------------------------------------------------------------------------------------------
+# low-precision latent cache  ([IPM] "Which Models Use MLA and What Is Next": MXFP4
+# quantisation of the KV cache data type; the formats themselves are those of the OCP
+# Microscaling Formats (MX) specification v1.0, which the pages do not restate)
+#
+#   [IPM]  "Multi-Head Latent Attention (MLA) Explained: What DeepSeek's Architecture Means
+#          for AI Inference Costs" (institutepm knowledge hub).
+#
+# A cached row of W numbers is cut into blocks of 32 consecutive elements.  Each block keeps
+# one shared scale 2^e (an E8M0 byte, e + 127) and 32 element codes: E4M3 bytes (MXFP8) or
+# E2M1 nibbles (MXFP4).  The dequantised value of element i of a block is 2^e * elem(code_i).
+# Readings (the pages name the format family only): the elements of a row are quantised in
+# the order [c_kv | rotated k_rope]; the block exponent is the smallest e with
+# max |v| <= max_elem * 2^e, i.e. the specification's floor(log2(max |v|)) - emax_elem,
+# raised by one when the block's largest element would otherwise saturate (so no element is
+# clipped), clamped to the E8M0 range [-127, 127] (a zero block gets e = -127); element codes
+# round to nearest, ties to the even code, and saturate at the largest finite magnitude (only
+# reachable at the clamp); a negative value that rounds to zero keeps its sign bit.
+# ------------------------------------------------------------------------------------------
+
+MX_BLOCK = 32
+
+# element formats: exponent bits, mantissa bits, exponent bias, emax (exponent of the
+# largest normal binade) and the largest finite magnitude
+MX_FORMATS = {
+    "e4m3": dict(ebits=4, mbits=3, bias=7, emax=8, max=448.0),
+    "e2m1": dict(ebits=2, mbits=1, bias=1, emax=2, max=6.0),
+}
+
+
+def fp_element_value(code: int, fmt: str) -> float:
+    """Value of one element code.  E4M3 (byte): S.EEEE.MMM, bias 7, no infinities,
+    S.1111.111 is NaN.  E2M1 (nibble): S.EE.M, bias 1, every code finite.  Exponent field 0
+    encodes subnormals 2^(1-bias) * M / 2^mbits."""
+    f = MX_FORMATS[fmt]
+    nbits = 1 + f["ebits"] + f["mbits"]
+    code = int(code) & ((1 << nbits) - 1)
+    sign = -1.0 if code >> (nbits - 1) else 1.0
+    E = (code >> f["mbits"]) & ((1 << f["ebits"]) - 1)
+    M = code & ((1 << f["mbits"]) - 1)
+    if fmt == "e4m3" and E == 15 and M == 7:
+        return float("nan")
+    if E == 0:
+        return sign * 2.0 ** (1 - f["bias"]) * M / 2 ** f["mbits"]
+    return sign * 2.0 ** (E - f["bias"]) * (1.0 + M / 2 ** f["mbits"])
+
+
+def fp_element_encode(v: float, fmt: str) -> int:
+    """Code of the representable value nearest to v (ties to the even code), saturating at
+    +/- max.  Walks the non-negative finite codes, which increase with their value."""
+    f = MX_FORMATS[fmt]
+    nbits = 1 + f["ebits"] + f["mbits"]
+    sign_bit = 1 << (nbits - 1)
+    v = float(v)
+    neg = v < 0 or (v == 0 and math.copysign(1.0, v) < 0)
+    a = abs(v)
+    n_finite = sign_bit - 1 if fmt == "e4m3" else sign_bit  # e4m3 drops S.1111.111 (NaN)
+    if a >= f["max"]:
+        mag = n_finite - 1
+    else:
+        mag = 0
+        while fp_element_value(mag + 1, fmt) <= a:
+            mag += 1
+        lo, hi = fp_element_value(mag, fmt), fp_element_value(mag + 1, fmt)
+        if a - lo > hi - a or (a - lo == hi - a and mag % 2 == 1):
+            mag += 1
+    return (sign_bit if neg else 0) | mag
+
+
+def mx_block_exponent(block, fmt: str) -> int:
+    """Shared exponent of a block: the smallest e with max |v| <= max_elem * 2^e, clamped to
+    [-127, 127].  With e0 = floor(log2(max |v|)) - emax the scaled maximum lies in
+    [2^emax, 2^(emax+1)), so e is e0, or e0 + 1 when that scaled maximum exceeds max_elem."""
+    f = MX_FORMATS[fmt]
+    amax = float(np.max(np.abs(np.asarray(block, dtype=F64))))
+    if amax == 0.0:
+        return -127
+    _, ex = math.frexp(amax)  # amax = m * 2^ex with 0.5 <= m < 1, so floor(log2 amax) = ex - 1
+    e = ex - 1 - f["emax"]
+    if math.ldexp(amax, -e) > f["max"]:
+        e += 1
+    return int(min(127, max(-127, e)))
+
+
+def element_table(fmt: str) -> np.ndarray:
+    """Values of the non-negative finite codes 0, 1, 2, ... (increasing with the code)."""
+    f = MX_FORMATS[fmt]
+    n = (1 << (f["ebits"] + f["mbits"])) - (1 if fmt == "e4m3" else 0)
+    return np.asarray([fp_element_value(c, fmt) for c in range(n)], dtype=F64)
+
+
+def fp_elements_encode(values, fmt: str) -> np.ndarray:
+    """fp_element_encode over an array: the same nearest-even, saturating choice, found by a
+    search of the increasing table instead of a walk."""
+    f = MX_FORMATS[fmt]
+    nbits = 1 + f["ebits"] + f["mbits"]
+    tab = element_table(fmt)
+    v = np.asarray(values, dtype=F64)
+    a = np.abs(v)
+    lo = np.clip(np.searchsorted(tab, a, side="right") - 1, 0, len(tab) - 1)
+    hi = np.minimum(lo + 1, len(tab) - 1)
+    dlo, dhi = a - tab[lo], tab[hi] - a
+    up = (hi > lo) & ((dlo > dhi) | ((dlo == dhi) & (lo % 2 == 1)))
+    mag = np.where(a >= f["max"], len(tab) - 1, np.where(up, hi, lo))
+    neg = np.signbit(v)
+    return np.where(neg, (1 << (nbits - 1)) | mag, mag).astype(np.int64)
+
+
+def mx_encode_rows(rows, fmt: str):
+    """Encode rows [..., W] (W a multiple of 32).  Returns (codes [..., W] ints, scale bytes
+    [..., W/32] ints); the scale byte of a block is its exponent e + 127."""
+    rows = np.asarray(rows, dtype=F64)
+    W = rows.shape[-1]
+    assert W % MX_BLOCK == 0
+    blocks = rows.reshape(-1, W // MX_BLOCK, MX_BLOCK)
+    e = np.empty(blocks.shape[:2], dtype=np.int64)
+    for i in range(blocks.shape[0]):
+        for b in range(blocks.shape[1]):
+            e[i, b] = mx_block_exponent(blocks[i, b], fmt)
+    scaled = np.ldexp(blocks, -e[..., None])
+    codes = fp_elements_encode(scaled, fmt).reshape(rows.shape)
+    return codes, (e + 127).reshape(rows.shape[:-1] + (W // MX_BLOCK,))
+
+
+def mx_decode_rows(codes, scale_bytes, fmt: str) -> np.ndarray:
+    """Dequantise rows: element i of block b is 2^(scale_bytes[b] - 127) * elem(codes[i])."""
+    codes = np.asarray(codes, dtype=np.int64)
+    f = MX_FORMATS[fmt]
+    nbits = 1 + f["ebits"] + f["mbits"]
+    value_of = np.asarray([fp_element_value(c, fmt) for c in range(1 << nbits)], dtype=F64)
+    e = np.asarray(scale_bytes, dtype=np.int64) - 127
+    return np.ldexp(value_of[codes], np.repeat(e, MX_BLOCK, axis=-1))
+
+
+def mx_pack_e2m1(codes) -> np.ndarray:
+    """Two E2M1 codes per byte: element 2i in the low nibble of byte i, 2i+1 in the high."""
+    c = np.asarray(codes, dtype=np.int64)
+    return ((c[0::2] & 0xF) | ((c[1::2] & 0xF) << 4)).astype(np.uint8)
+
+
+def mx_unpack_e2m1(packed) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.int64)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int64)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = (p >> 4) & 0xF
+    return out

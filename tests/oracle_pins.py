@@ -297,4 +297,106 @@ def pin_paged_gather(O):
         assert np.array_equal(rows[t], pool[[3, 0, 4][t // 4], t % 4])
 
 
+# ------------------------------------------------------------------------------ MX cache formats
+
+def pin_e4m3_table(O):
+    """Every E4M3 code decodes as torch's float8_e4m3fn does (a library routine), and the
+    OCP 8-bit format's landmarks hold: 448 largest, 2^-6 smallest normal, 2^-9 smallest
+    subnormal, S.1111.111 NaN."""
+    import torch
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.asarray([O.fp_element_value(c, "e4m3") for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and int(np.isnan(got).sum()) == 2
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert O.fp_element_value(0x7E, "e4m3") == 448.0 and O.fp_element_value(0x08, "e4m3") == 2.0 ** -6
+    assert O.fp_element_value(0x01, "e4m3") == 2.0 ** -9 and O.fp_element_value(0x38, "e4m3") == 1.0
+    assert O.fp_element_value(0xB8, "e4m3") == -1.0
+
+
+def pin_e2m1_table(O):
+    """The sixteen E2M1 values of the OCP MX specification's FP4 element table."""
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = [O.fp_element_value(c, "e2m1") for c in range(16)]
+    assert got[:8] == want and got[8:] == [-v for v in want]
+
+
+def pin_element_rounding(O):
+    """Round to nearest, ties to the even code, saturating: E4M3 against torch's
+    float32 -> float8_e4m3fn conversion (RNE) inside the finite range, hand-worked E2M1
+    ties, and the array form equal to the scalar definition."""
+    import torch
+    r = np.random.default_rng(7)
+    v = np.concatenate([r.standard_normal(400) * 60.0, r.standard_normal(200) * 2.0 ** -7,
+                        (O.element_table("e4m3")[:-1] + O.element_table("e4m3")[1:]) / 2])
+    v = np.concatenate([v, -v]).astype(np.float32).astype(np.float64)
+    v = v[np.abs(v) < 448.0]
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.asarray([O.fp_element_encode(x, "e4m3") for x in v])
+    assert np.array_equal(got, ref.astype(np.int64))
+    assert O.fp_element_encode(1000.0, "e4m3") == 0x7E and O.fp_element_encode(-500.0, "e4m3") == 0xFE
+    # E2M1: midpoints go to the even code; beyond 6 saturates; -0.1 keeps its sign bit
+    cases = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6, 7.0: 7, 100.0: 7,
+             0.26: 1, 2.49: 4, 2.51: 5, -0.1: 8, -3.4: 13, -5.1: 15}
+    for x, c in cases.items():
+        assert O.fp_element_encode(x, "e2m1") == c, (x, c)
+    for fmt in ("e4m3", "e2m1"):
+        w = np.concatenate([v / (1.0 if fmt == "e4m3" else 70.0), [0.0, -0.0]])
+        assert np.array_equal(O.fp_elements_encode(w, fmt), [O.fp_element_encode(x, fmt) for x in w])
+
+
+def pin_mx_block_exponent(O):
+    """The block exponent is the smallest e with max|v| <= max_elem * 2^e (hand-worked
+    cases), -127 for a zero block, and scales with the block: 2^k * block -> e + k."""
+    assert O.mx_block_exponent([1.0, -0.5], "e4m3") == -8      # 1 * 2^8 = 256 <= 448
+    assert O.mx_block_exponent([1.75], "e4m3") == -8           # 448 exactly
+    assert O.mx_block_exponent([-1.76], "e4m3") == -7          # 450.56 > 448
+    assert O.mx_block_exponent([1.5], "e2m1") == -2            # 6 exactly
+    assert O.mx_block_exponent([1.6], "e2m1") == -1
+    assert O.mx_block_exponent([0.0, -0.0], "e4m3") == -127
+    r = np.random.default_rng(3)
+    for fmt in ("e4m3", "e2m1"):
+        blk = r.standard_normal(32)
+        for k in (-20, -3, 5, 40):
+            assert O.mx_block_exponent(np.ldexp(blk, k), fmt) == O.mx_block_exponent(blk, fmt) + k
+        rows = r.standard_normal((2, 64))
+        c0, s0 = O.mx_encode_rows(rows, fmt)
+        c1, s1 = O.mx_encode_rows(np.ldexp(rows, 9), fmt)
+        assert np.array_equal(c0, c1) and np.array_equal(s1, s0 + 9)
+
+
+def pin_mx_round_trip_and_bound(O):
+    """Dequantised values re-encode to themselves exactly; encoding a real row errs by at
+    most half the element grid's spacing at the scaled magnitude; blocks are 32 wide."""
+    r = np.random.default_rng(11)
+    for fmt, top in (("e4m3", 0x7E), ("e2m1", 7)):
+        f = O.MX_FORMATS[fmt]
+        sign = 0x80 if fmt == "e4m3" else 0x8
+        codes = r.integers(0, top + 1, size=(3, 96)) | (r.integers(0, 2, size=(3, 96)) * sign)
+        scales = r.integers(100, 150, size=(3, 3))
+        vals = O.mx_decode_rows(codes, scales, fmt)
+        for b in range(3):   # block b of every row uses scales[:, b] and nothing else
+            blk = vals[:, 32 * b:32 * b + 32]
+            assert np.array_equal(blk, np.ldexp(np.vectorize(lambda c: O.fp_element_value(c, fmt))(
+                codes[:, 32 * b:32 * b + 32]), scales[:, b:b + 1] - 127))
+        c2, s2 = O.mx_encode_rows(vals, fmt)
+        assert np.array_equal(O.mx_decode_rows(c2, s2, fmt), vals)
+        x = r.standard_normal((4, 64)) * np.exp(r.standard_normal((4, 1)) * 3)
+        c, s = O.mx_encode_rows(x, fmt)
+        e = np.repeat(s - 127, 32, axis=-1)
+        a = np.abs(np.ldexp(x, -e))
+        assert np.all(a <= f["max"])
+        min_normal = 2.0 ** (1 - f["bias"])
+        binade = np.floor(np.log2(np.maximum(a, min_normal)))
+        half_step = np.ldexp(2.0 ** (binade - f["mbits"] - 1), e)
+        assert np.all(np.abs(O.mx_decode_rows(c, s, fmt) - x) <= half_step)
+
+
+def pin_e2m1_packing(O):
+    """Two E2M1 codes per byte, element 2i in the low nibble: codes (2, 4), i.e. 1.0 then
+    2.0, pack to 0x42."""
+    assert list(O.mx_pack_e2m1([2, 4, 15, 0])) == [0x42, 0x0F]
+    assert list(O.mx_unpack_e2m1(np.asarray([0x42, 0x0F]))) == [2, 4, 15, 0]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

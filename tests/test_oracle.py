@@ -141,6 +141,44 @@ def _gather_wrong_slot(pool, pt_row, length):
                       dtype=np.float64)
 
 
+def _mx_exponent_floor_only(block, fmt):
+    # the specification's floor rule without the raise: large elements saturate
+    a = float(np.max(np.abs(np.asarray(block, dtype=np.float64))))
+    if a == 0.0:
+        return -127
+    return int(max(-127, min(127, math.frexp(a)[1] - 1 - OR.MX_FORMATS[fmt]["emax"])))
+
+
+def _encode_ties_away(v, fmt):
+    c = OR.fp_element_encode(v, fmt)
+    lo = OR.fp_element_value(c, fmt)
+    nxt = c + 1
+    if abs(abs(v) - abs(lo)) > 0 and (c & 1) == 0:
+        hi = OR.fp_element_value(nxt, fmt) if not math.isnan(OR.fp_element_value(nxt, fmt)) else lo
+        if abs(abs(v) - abs(lo)) == abs(abs(hi) - abs(v)):
+            return nxt
+    return c
+
+
+def _e4m3_bias8(code, fmt):
+    v = OR.fp_element_value(code, fmt)
+    return v / 2.0 if fmt == "e4m3" else v
+
+
+def _pack_swapped(codes):
+    c = np.asarray(codes, dtype=np.int64)
+    return ((c[1::2] & 0xF) | ((c[0::2] & 0xF) << 4)).astype(np.uint8)
+
+
+def _decode_blocks_of_16(codes, scale_bytes, fmt):
+    codes = np.asarray(codes, dtype=np.int64)
+    vals = np.vectorize(lambda c: OR.fp_element_value(c, fmt))(codes).astype(np.float64)
+    e = np.asarray(scale_bytes, dtype=np.int64) - 127
+    e = np.repeat(e, 16, axis=-1)
+    e = np.concatenate([e, np.repeat(e[..., -1:], codes.shape[-1] - e.shape[-1], axis=-1)], axis=-1)
+    return np.ldexp(vals, e[..., :codes.shape[-1]])
+
+
 MUTANTS = {
     "rope_sign_flip": dict(rope_rotate=_rope_sign_flip),
     "rope_half_split": dict(rope_rotate=_rope_half_split),
@@ -157,6 +195,11 @@ MUTANTS = {
     "mha_count_drops_v": dict(mha_numbers_per_token=_mha_numbers_single),
     "paged_gather_wrong_slot": dict(sequence_rows=_gather_wrong_slot),
     "default_scale_sqrt_dh": dict(default_scale=_scale_sqrt_dh),
+    "mx_exponent_floor_only": dict(mx_block_exponent=_mx_exponent_floor_only),
+    "mx_ties_away_from_zero": dict(fp_element_encode=_encode_ties_away),
+    "e4m3_bias_8": dict(fp_element_value=_e4m3_bias8),
+    "e2m1_nibbles_swapped": dict(mx_pack_e2m1=_pack_swapped),
+    "mx_decode_blocks_of_16": dict(mx_decode_rows=_decode_blocks_of_16),
 }
 
 
