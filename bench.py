@@ -46,9 +46,21 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def row_bytes(case) -> int:
+    """Bytes of one cached row: W bf16 numbers, or an MX row (W codes of 1 byte for MXFP8, of
+    half a byte for MXFP4, plus one scale byte per 32-element block)."""
+    s = case["shape"]
+    kv = case.get("kv", "")
+    if kv == "mxfp8":
+        return s.width + s.width // 32
+    if kv == "mxfp4":
+        return s.width // 2 + s.width // 32
+    return s.width * 2
+
+
 def workload_numbers(case):
     """Algorithmic bytes and FLOPs of one attention launch (the split-attention kernel).
-    Decode: cache rows read once (L*W*2), queries (n_h*W*2), outputs (n_h*(d_c*2+4)) per
+    Decode: cache rows read once (L*row_bytes: L*W*2 for bf16), queries (n_h*W*2), outputs (n_h*(d_c*2+4)) per
     sequence; FLOPs 2*L*n_h*(W + d_c) per sequence (scores plus weighted sum).
     Causal prefill of T queries: the T cache rows once, T queries and outputs; query i
     attends i+1 tokens, so FLOPs 2*n_h*(W + d_c)*T(T+1)/2."""
@@ -59,16 +71,17 @@ def workload_numbers(case):
         T = int(case["T"])
         return T * Wd * 2 + T * per_q, s.n_heads * (Wd + s.d_latent) * T * (T + 1)
     L = case["seq_lens"].astype(np.int64)
-    bytes_ = int(np.sum(L * Wd * 2 + per_q))
+    bytes_ = int(np.sum(L * row_bytes(case) + per_q))
     flops = int(np.sum(2 * L * s.n_heads * (Wd + s.d_latent)))
     return bytes_, flops
 
 
 # the sources each profiled kernel is compiled from (its own header and the headers it includes)
 KERNEL_SOURCES = {
-    "tc_attention": ["tc_attention.cuh", "tc_ptx.cuh", "sched.cuh", "mla_common.cuh", "simt_attention.cuh"],
-    "simt_attention": ["simt_attention.cuh", "sched.cuh", "mla_common.cuh"],
-    "tc_gemm": ["tc_gemm.cuh", "tc_ptx.cuh", "mla_common.cuh"],
+    "tc_attention": ["tc_attention.cuh", "tc_ptx.cuh", "sched.cuh", "mla_common.cuh", "simt_attention.cuh",
+                     "mx_format.cuh"],
+    "simt_attention": ["simt_attention.cuh", "sched.cuh", "mla_common.cuh", "mx_format.cuh"],
+    "tc_gemm": ["tc_gemm.cuh", "tc_ptx.cuh", "mla_common.cuh", "mx_format.cuh"],
 }
 
 
@@ -185,7 +198,6 @@ def cpu_oracle_sample(case, seqs, out_proj: bool = False, heads=None):
     s = case["shape"]
     h = s.n_heads if heads is None else heads
     sc = O.default_scale(s.d_nope, s.d_rope)
-    pool = case["pool"]
     f = lambda a: W.to_f64(a, case["dtype"])  # noqa: E731
     w_uk, w_uv = f(case["w_uk"][:, :h * s.d_nope]), f(case["w_uv"][:, :h * s.d_nope])
     w_o = f(case["w_o"][:h * s.d_nope]) if out_proj else None
@@ -197,13 +209,27 @@ def cpu_oracle_sample(case, seqs, out_proj: bool = False, heads=None):
         if appending:
             O.latent_kv(f(case["x"][b:b + 1]), w_dkv, w_kr, case["append_pos"][b:b + 1], s.rope_base)
         L = int(case["seq_lens"][b])
-        rows = W.to_f64(W.gather_rows(pool, case["page_table"][b], L), case["dtype"])
+        rows = oracle_rows(case, b, L)
         q_r = O.rope_rotate(f(case["q_rope"][b][:h]), case["pos"][b], s.rope_base)
         o = O.attention_unabsorbed(f(case["q_nope"][b][:h]), q_r, rows[:, :s.d_latent], rows[:, s.d_latent:],
                                    w_uk, w_uv, sc)[0]
         if out_proj:
             O.output_projection(o.reshape(1, -1), w_o)
     return time.perf_counter() - t0
+
+
+def oracle_rows(case, b: int, L: int):
+    """The oracle's float64 view of sequence b's first L cached rows (an MX cache through the
+    oracle's MX decoder)."""
+    import oracle.mla_oracle as O
+    kv = case.get("kv", "")
+    if not kv:
+        return W.to_f64(W.gather_rows(case["pool"], case["page_table"][b], L), case["dtype"])
+    codes = W.gather_rows(case["codes"], case["page_table"][b], L).astype(np.int64)
+    sc = W.gather_rows(case["scales"], case["page_table"][b], L).astype(np.int64)
+    if kv == "mxfp4":
+        codes = O.mx_unpack_e2m1(codes)
+    return O.mx_decode_rows(codes, sc, "e4m3" if kv == "mxfp8" else "e2m1")
 
 
 def oracle_sample_text(case, n_seq: int, n_all: int, heads: int, per_step: bool = False) -> str:
@@ -281,7 +307,8 @@ def config_of(name, case, out_proj=False):
     return {"workload": name, "batch": int(case["seq_lens"].shape[0]), **extra,
             "seq_len": int(case["seq_lens"].max()), "n_heads": s.n_heads, "d_nope": s.d_nope,
             "d_rope": s.d_rope, "d_latent": s.d_latent, "page_size": s.page_size,
-            "page_table": "shuffled",
+            "page_table": "shuffled", "cache": {"": "bf16 rows", "mxfp8": "MXFP8 (E4M3, 32-element E8M0 blocks)",
+                                                 "mxfp4": "MXFP4 (E2M1, 32-element E8M0 blocks)"}[w.kv],
             "l2": "flushed between steps (256 MB write, then read back so no dirty lines remain)"}
 
 
@@ -316,7 +343,12 @@ def run_ours(args):
     dt = case["dtype"]
     dev = lambda a: W.to_device(a, dt)  # noqa: E731
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()  # noqa: E731
-    cache = M.PagedCache(dev(case["pool"]), i32(case["page_table"]), i32(case["seq_lens"]))
+    if case.get("kv"):
+        kvf = {"mxfp8": M.MLA_KV_MXFP8, "mxfp4": M.MLA_KV_MXFP4}[case["kv"]]
+        cache = M.PagedCache(torch.from_numpy(case["codes"]).cuda(), i32(case["page_table"]),
+                             i32(case["seq_lens"]), kvf, torch.from_numpy(case["scales"]).cuda())
+    else:
+        cache = M.PagedCache(dev(case["pool"]), i32(case["page_table"]), i32(case["seq_lens"]))
     q_nope, q_rope = dev(case["q_nope"]), dev(case["q_rope"])
     prefill = mode == "prefill"
     pos = i32(case["append_pos"] if prefill else case["pos"])

@@ -12,6 +12,8 @@
  *         MLA pairs with PagedAttention.
  *   [RMJ] "Multi-Head Latent Attention and the Compression of the KV Cache": by associativity
  *         the up-projection is absorbed into the query, so attention runs on the latent.
+ *   [IPM] "Multi-Head Latent Attention (MLA) Explained": MXFP4 quantisation of the KV cache
+ *         (section "Which Models Use MLA and What Is Next").
  *
  * Notation: n_h heads, d_h (= d_nope) per-head width, d_r (= d_rope) RoPE width, d_c latent
  * width, W = d_c + d_r numbers cached per token, P = page_size tokens per page.
@@ -29,8 +31,8 @@
  *     shapes given below (no strides).
  *   - RoPE rotates interleaved pairs (2i, 2i+1) by pos * rope_base^(-2i/d_r); positions are
  *     0-based.  The score scale is cfg->softmax_scale, or 1/sqrt(d_h + d_r) when it is 0.
- *   - Slots of the pool that no token owns must hold finite values (masked tokens still
- *     meet a zero weight: 0 * finite = 0).
+ *   - Slots of a plain pool that no token owns must hold finite values (masked tokens still
+ *     meet a zero weight: 0 * finite = 0).  An MX cache has no such rule.
  *   - lse is the natural-log log-sum-exp of the scaled scores of one (query, head).
  *   - Kernels are launched with programmatic dependent launch: a kernel of this library may
  *     start while the kernel before it in the stream finishes, if that kernel allows it
@@ -91,21 +93,42 @@ typedef struct {
     int32_t dtype;         /* mla_dtype                               */
 } mla_config;
 
+/* Element format of the cached rows.
+ * MLA_KV_PLAIN: rows of cfg->dtype numbers.
+ * MLA_KV_MXFP8 / MLA_KV_MXFP4: the low-precision cache that [IPM] names (MXFP4 quantisation
+ *   of the KV cache), in the block formats of the OCP Microscaling (MX) specification v1.0.
+ *   A row of W numbers is cut into W/32 blocks of 32 consecutive elements; each block has one
+ *   E8M0 scale byte s (the power of two 2^(s-127)) and 32 element codes, E4M3 bytes (MXFP8)
+ *   or E2M1 nibbles (MXFP4; element 2i in the low nibble of byte i).  Element i of block k
+ *   of a row stands for 2^(s_k - 127) * value(code_i).  W must be a multiple of 32.
+ *   mla_cache_append encodes: block exponent e = the smallest integer with
+ *   max|v| <= max_elem * 2^e (max_elem 448 for E4M3, 6 for E2M1), clamped to [-127, 127];
+ *   codes round v * 2^-e to nearest, ties to even (the fp32 row after RoPE is the input).
+ *   Unlike a plain cache, slots that no token owns may hold any bytes.
+ *   [IPM] "Multi-Head Latent Attention (MLA) Explained: What DeepSeek's Architecture Means
+ *         for AI Inference Costs", section "Which Models Use MLA and What Is Next". */
+typedef enum { MLA_KV_PLAIN = 0, MLA_KV_MXFP8 = 1, MLA_KV_MXFP4 = 2 } mla_kv_format;
+
 /* Paged latent cache ([GLO]: MLA pairs with PagedAttention; [OPN] s.3: only c_kv is cached,
  * here with the RoPE key beside it).  Token t of sequence b lives in row
  * pool[page_table[b*max_pages + t/P]][t%P][0:W]: columns [0,d_c) hold c_kv, [d_c,W) the
  * rotated RoPE key. */
 typedef struct {
-    void* pool;                 /* device [num_pages, P, W], cfg->dtype                 */
+    void* pool;                 /* device [num_pages, P, W] of cfg->dtype (MLA_KV_PLAIN), or
+                                   the codes: [num_pages, P, W] bytes (MXFP8),
+                                   [num_pages, P, W/2] bytes (MXFP4)                    */
     int64_t num_pages;
     const int32_t* page_table;  /* device [batch, max_pages] physical page ids         */
     int32_t max_pages;
     int32_t batch;
     const int32_t* seq_lens;    /* device [batch]: cached tokens of each sequence       */
+    int32_t kv_format;          /* mla_kv_format (0 for a plain cache)                  */
+    void* kv_scales;            /* MX formats: device [num_pages, P, W/32] scale bytes,
+                                   16-byte aligned; unused (may be NULL) for a plain cache */
 } mla_cache;
 
 /* Build identification: returns MLA_ABI_VERSION. */
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 MLA_API int32_t mla_abi_version(void);
 
 /* Short English text for a status code (static storage). */
@@ -118,6 +141,9 @@ MLA_API const char* mla_status_string(mla_status status);
  * x       device [n_tokens, d_model]
  * w_dkv   device [d_model, d_c]       w_kr device [d_model, d_r]
  * seq_idx device int32 [n_tokens]     pos  device int32 [n_tokens]
+ * An MX cache (cache->kv_format) receives the row's codes and block scale bytes instead; that
+ * needs cfg->dtype == MLA_BF16 and the tensor-core path (n_h = 128, d_c = 512, d_r = 64, d_model
+ * a multiple of 64 on sm_103; else MLA_ERR_UNSUPPORTED).
  * Tokens must target distinct rows.  seq_lens is not modified (the caller owns lengths).
  * A seq_idx outside [0,batch), a position outside the page table or a page id outside the
  * pool sets MLA_ERR_DEVICE_BOUNDS and that token is skipped.  n_tokens == 0 is a no-op. */
@@ -148,6 +174,9 @@ MLA_API mla_status mla_workspace_size(const mla_config* cfg, size_t* bytes);
  * q_cat device [batch, n_h, W]; o_lat device [batch, n_h, d_c]; lse device float [batch, n_h].
  * The work is split over the sequence length and merged by a log-sum-exp combine.
  * A sequence with seq_lens[b] == 0 yields o_lat = 0 and lse = -inf.
+ * An MX cache is read as its dequantised rows (exactly: every dequantised value is a bf16 number
+ * in the range the scales of real data give), so the formulas above hold with pool_row the
+ * dequantised row.
  * workspace: device, at least mla_workspace_size() bytes (else MLA_ERR_WORKSPACE). */
 MLA_API mla_status mla_decode(const mla_config* cfg, const mla_cache* cache, const void* q_cat,
                       void* o_lat, float* lse, void* workspace, size_t workspace_bytes,

@@ -13,7 +13,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import MLAError, MLA_F32, MLA_BF16  # noqa: F401
+from ._lib import MLAError, MLA_F32, MLA_BF16, MLA_KV_PLAIN, MLA_KV_MXFP8, MLA_KV_MXFP4  # noqa: F401
 
 __all__ = ["MLAConfig", "PagedCache", "mla_cache_append", "mla_absorb_q", "mla_workspace_size",
            "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_out_proj", "mla_query_proj",
@@ -62,15 +62,19 @@ class MLAConfig:
 @dataclass
 class PagedCache:
     """Caller-owned paged latent cache: pool [num_pages, P, W], page_table [B, max_pages]
-    int32, seq_lens [B] int32 (all device tensors)."""
+    int32, seq_lens [B] int32 (all device tensors).  An MX cache (kv_format MLA_KV_MXFP8 or
+    MLA_KV_MXFP4) holds uint8 codes in `pool` ([num_pages, P, W] or [num_pages, P, W/2]) and
+    the block scale bytes in `kv_scales` ([num_pages, P, W/32] uint8)."""
     pool: torch.Tensor
     page_table: torch.Tensor
     seq_lens: torch.Tensor
+    kv_format: int = MLA_KV_PLAIN
+    kv_scales: torch.Tensor = None
 
     def c(self) -> _lib.MlaCache:
         return _lib.MlaCache(self.pool.data_ptr(), self.pool.shape[0], self.page_table.data_ptr(),
                              self.page_table.shape[1], self.page_table.shape[0],
-                             self.seq_lens.data_ptr())
+                             self.seq_lens.data_ptr(), self.kv_format, _ptr(self.kv_scales))
 
 
 def _stream(stream) -> int:

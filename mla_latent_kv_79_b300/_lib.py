@@ -17,6 +17,7 @@ MLA_F32, MLA_BF16 = 0, 1
 MLA_TUNE_ATTN_UNITS, MLA_TUNE_FORCE_SIMT, MLA_TUNE_WAIT_LIMIT_US = 0, 1, 2
 MLA_TUNE_GEMM_HEADS, MLA_TUNE_GEMM_STAGES, MLA_TUNE_NO_PDL, MLA_TUNE_SCHEDULE = 3, 4, 5, 6
 MLA_TUNE_GEMM_KSPLIT = 7
+MLA_KV_PLAIN, MLA_KV_MXFP8, MLA_KV_MXFP4 = 0, 1, 2
 
 
 class MlaConfig(ctypes.Structure):
@@ -29,7 +30,8 @@ class MlaConfig(ctypes.Structure):
 class MlaCache(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
                 ("page_table", ctypes.c_void_p), ("max_pages", ctypes.c_int32),
-                ("batch", ctypes.c_int32), ("seq_lens", ctypes.c_void_p)]
+                ("batch", ctypes.c_int32), ("seq_lens", ctypes.c_void_p),
+                ("kv_format", ctypes.c_int32), ("kv_scales", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p

@@ -44,9 +44,12 @@ static mla_status device_info(DeviceInfo** out) {
                 (const void*)simt_gemm_kernel<bf16, EPI_STORE>, (const void*)simt_gemm_kernel<float, EPI_STORE>,
                 (const void*)simt_gemm_kernel<bf16, EPI_APPEND>, (const void*)simt_gemm_kernel<float, EPI_APPEND>,
                 (const void*)rope_query_kernel<bf16>, (const void*)rope_query_kernel<float>,
-                (const void*)simt_attention_kernel<bf16>, (const void*)simt_attention_kernel<float>,
+                (const void*)simt_attention_kernel<bf16, KV_PLAIN>, (const void*)simt_attention_kernel<float, KV_PLAIN>,
+                (const void*)simt_attention_kernel<bf16, KV_MXFP8>, (const void*)simt_attention_kernel<float, KV_MXFP8>,
+                (const void*)simt_attention_kernel<bf16, KV_MXFP4>, (const void*)simt_attention_kernel<float, KV_MXFP4>,
                 (const void*)combine_kernel<bf16>, (const void*)combine_kernel<float>,
-                (const void*)tca::tc_attention_kernel, (const void*)tcg::tc_gemm_kernel<tcg::ABSORB>,
+                (const void*)tca::tc_attention_kernel<KV_PLAIN>, (const void*)tca::tc_attention_kernel<KV_MXFP8>,
+                (const void*)tca::tc_attention_kernel<KV_MXFP4>, (const void*)tcg::tc_gemm_kernel<tcg::ABSORB>,
                 (const void*)tcg::tc_gemm_kernel<tcg::OUT>, (const void*)tcg::tc_gemm_kernel<tcg::APPEND>,
                 (const void*)tcg::tc_gemm_kernel<tcg::OPROJ>};
             for (const void* f : fns)
@@ -94,6 +97,11 @@ static mla_status check_cache(const mla_config* c, const mla_cache* k) {
     if (!k || !k->pool || !k->page_table || k->num_pages <= 0 || k->max_pages <= 0 || k->batch <= 0)
         return MLA_ERR_INVALID_ARG;
     if (!aligned16(k->pool)) return MLA_ERR_INVALID_ARG;
+    if (k->kv_format != MLA_KV_PLAIN) {
+        if (k->kv_format != MLA_KV_MXFP8 && k->kv_format != MLA_KV_MXFP4) return MLA_ERR_INVALID_ARG;
+        if (!k->kv_scales || !aligned16(k->kv_scales)) return MLA_ERR_INVALID_ARG;
+        if ((c->d_latent + c->d_rope) % MX_BLOCK) return MLA_ERR_UNSUPPORTED;
+    }
     if ((long long)k->max_pages * c->page_size > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
     return MLA_OK;
 }
@@ -120,6 +128,12 @@ static tcg::Tuning gemm_tuning(unsigned long long wait_ns) {
 }
 
 // ----------------------------------------------------------------------------- attention
+template <typename T, int KVF>
+static void launch_simt_attention(dim3 grid, size_t smem, cudaStream_t stream, const AttnArgs& a, int hg) {
+    cudaFuncSetAttribute(simt_attention_kernel<T, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    simt_attention_kernel<T, KVF><<<grid, 256, smem, stream>>>(a, hg);
+}
+
 static mla_status attention(const mla_config* cfg, const mla_cache* cache, QuerySet qs,
                             const void* q_cat, void* o_lat, float* lse, void* ws, size_t ws_bytes,
                             cudaStream_t stream) {
@@ -139,6 +153,7 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
     a.qs = qs;
     a.q_cat = q_cat;
     a.pool = cache->pool;
+    a.scales = cache->kv_scales;
     a.page_table = cache->page_table;
     a.max_pages = cache->max_pages;
     a.num_pages = cache->num_pages;
@@ -175,11 +190,17 @@ static mla_status attention(const mla_config* cfg, const mla_cache* cache, Query
         dim3 grid(U, (n_h + hg - 1) / hg);
         if (timed) cudaEventRecord(g_ev_before, stream);
         if (cfg->dtype == MLA_BF16) {
-            cudaFuncSetAttribute(simt_attention_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            simt_attention_kernel<bf16><<<grid, 256, smem, stream>>>(a, hg);
+            switch (cache->kv_format) {
+                case MLA_KV_MXFP8: launch_simt_attention<bf16, KV_MXFP8>(grid, smem, stream, a, hg); break;
+                case MLA_KV_MXFP4: launch_simt_attention<bf16, KV_MXFP4>(grid, smem, stream, a, hg); break;
+                default: launch_simt_attention<bf16, KV_PLAIN>(grid, smem, stream, a, hg); break;
+            }
         } else {
-            cudaFuncSetAttribute(simt_attention_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            simt_attention_kernel<float><<<grid, 256, smem, stream>>>(a, hg);
+            switch (cache->kv_format) {
+                case MLA_KV_MXFP8: launch_simt_attention<float, KV_MXFP8>(grid, smem, stream, a, hg); break;
+                case MLA_KV_MXFP4: launch_simt_attention<float, KV_MXFP4>(grid, smem, stream, a, hg); break;
+                default: launch_simt_attention<float, KV_PLAIN>(grid, smem, stream, a, hg); break;
+            }
         }
         if (timed) cudaEventRecord(g_ev_after, stream);
         if ((st = launch_status()) != MLA_OK) return st;
@@ -271,8 +292,10 @@ mla_status mla_cache_append(const mla_config* cfg, const mla_cache* cache, const
     const int W = cfg->d_latent + cfg->d_rope;
     DeviceInfo* dev;
     if ((st = device_info(&dev)) != MLA_OK) return st;
-    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() && tc_gemm_append_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor) &&
-        (long long)cache->num_pages * cfg->page_size < (1LL << 31)) {
+    const bool tc_ok = tc_gemm_append_supported(cfg, n_tokens, dev->cc_major, dev->cc_minor) &&
+                       (long long)cache->num_pages * cfg->page_size < (1LL << 31);
+    if (cache->kv_format != MLA_KV_PLAIN && !tc_ok) return MLA_ERR_UNSUPPORTED;  // MX encoding: tensor-core path only
+    if ((!g_tune[MLA_TUNE_FORCE_SIMT].load() || cache->kv_format != MLA_KV_PLAIN) && tc_ok) {
         st = tc_gemm_append(cfg, cache, x, w_dkv, w_kr, seq_idx, pos, n_tokens,
                             gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull), s);
         if (st == MLA_OK) count_launches(1);

@@ -6,6 +6,7 @@
 // softmax) and accumulates o[h, :] += p[h, t] * c_kv[t, :].
 #pragma once
 
+#include "mx_format.cuh"
 #include "sched.cuh"
 
 namespace mla {
@@ -13,7 +14,8 @@ namespace mla {
 struct AttnArgs {
     QuerySet qs;
     const void* q_cat;          // [Q, n_h, W]
-    const void* pool;           // [num_pages, P, W]
+    const void* pool;           // [num_pages, P, W] elements, or the codes of an MX cache
+    const void* scales;         // MX cache: [num_pages, P, W / 32] E8M0 scale bytes
     const int* page_table;      // [batch, max_pages]
     int max_pages;
     long long num_pages;
@@ -42,7 +44,9 @@ __host__ __device__ inline size_t simt_attn_smem_bytes(int hg, int width, int d_
                             (size_t)hg * SIMT_TB + (size_t)hg * d_c + 3 * (size_t)hg);
 }
 
-template <typename T>
+// KVF: the cache's element format (KV_PLAIN rows of T, or an MX cache read as its dequantised
+// values).
+template <typename T, int KVF>
 __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg) {
     extern __shared__ float smem[];
     __shared__ long long red[SCHED_SCRATCH];
@@ -85,8 +89,14 @@ __global__ void __launch_bounds__(256) simt_attention_kernel(AttnArgs a, int hg)
                 float v = 0.f;
                 if (t < t_end) {
                     int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + t / ps);
-                    if (page >= 0 && page < a.num_pages)
-                        v = to_f32(pool[((long long)page * ps + t % ps) * W + k]);
+                    if (page >= 0 && page < a.num_pages) {
+                        const long long row = (long long)page * ps + t % ps;
+                        if (KVF == KV_PLAIN)
+                            v = to_f32(pool[row * W + k]);
+                        else
+                            v = mx_load<KVF>(reinterpret_cast<const uint8_t*>(a.pool) + row * mx_row_bytes(KVF, W),
+                                             reinterpret_cast<const uint8_t*>(a.scales) + row * mx_scale_bytes(W), k);
+                    }
                     else if (k == 0)
                         set_device_error(MLA_ERR_DEVICE_BOUNDS);
                 }

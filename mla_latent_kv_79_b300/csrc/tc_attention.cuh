@@ -39,6 +39,7 @@
 
 #include "sched.cuh"
 #include "simt_attention.cuh"
+#include "mx_format.cuh"
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -47,37 +48,61 @@ namespace tca {
 constexpr int NH = 128, DC = 512, DR = 64, WID = 576, PAGE = 64;
 constexpr int CHUNK = 64 * 128;                   // 64 rows x 64 bf16, 128-byte swizzled
 constexpr int LAT_CHUNKS = 8;
-constexpr int STAGES = 3;
+constexpr int MAX_STAGES = 3;
 constexpr int S_STAGE_BYTES = 9 * CHUNK;          // score CTA: whole page, 9 chunks (72 KB)
 constexpr int Q_ITEMS = 2;                        // ring items per query, nine 8 KB boxes each
 constexpr int V_STAGE_BYTES = LAT_CHUNKS * CHUNK; // value CTA: latent part (64 KB)
-constexpr int OFF_R = STAGES * V_STAGE_BYTES;     // value CTA: P buffers
 constexpr int P_BYTES = NH * 128;                 // P [128 heads x 64 tokens] bf16, SW128 K-major
 constexpr int META_BYTES = NH * 8;                // (alpha, l) per head, fp32
 constexpr int PBUF_BYTES = P_BYTES + META_BYTES;
 constexpr int R_BYTES = 2 * PBUF_BYTES;
-constexpr int OFF_BARS = OFF_R + R_BYTES;         // same offset in both CTAs
-static_assert(STAGES * S_STAGE_BYTES <= OFF_BARS, "score CTA stages must fit below the barriers");
+constexpr int HALF = 32;                          // MX caches: cache rows per raw item (half a page)
+constexpr int MAX_RAW = 6;
 enum {
-    B_FULL = 0,                  // [STAGES] page landed in this CTA's ring
-    B_EMPTY = B_FULL + STAGES,   // [STAGES] this CTA's consumer released the stage
-    B_SFULL = B_EMPTY + STAGES,  // [2] score CTA: S buffer written
-    B_SFREE = B_SFULL + 2,       // [2] score CTA: S buffer read by the 4 softmax warps
-    B_PFULL = B_SFREE + 2,       // [2] value CTA: P + meta landed (own expect_tx + bytes)
-    B_PEMPTY = B_PFULL + 2,      // [2] score CTA: value CTA's PV finished with P buffer b
-    B_PREADY = B_PEMPTY + 2,     // [2] value CTA: O rescaled, P buffer b ready for the MMA
-    B_PVDONE = B_PREADY + 2,     // [2] value CTA: PV of the page that used P buffer b complete
-    B_OFREE = B_PVDONE + 2,      // value CTA: O drained
-    B_DONE = B_OFREE + 1,        // MMA drain at exit
-    B_QREADY = B_DONE + 1,       // score CTA: the segment's query is in TMEM (4 softmax warps)
-    NBARS
+    B_FULL = 0,                      // [STAGES] page landed in this CTA's ring
+    B_EMPTY = B_FULL + MAX_STAGES,   // [STAGES] this CTA's consumer released the stage
+    B_SFULL = B_EMPTY + MAX_STAGES,  // [2] score CTA: S buffer written
+    B_SFREE = B_SFULL + 2,           // [2] score CTA: S buffer read by the 4 softmax warps
+    B_PFULL = B_SFREE + 2,           // [2] value CTA: P + meta landed (own expect_tx + bytes)
+    B_PEMPTY = B_PFULL + 2,          // [2] score CTA: value CTA's PV finished with P buffer b
+    B_PREADY = B_PEMPTY + 2,         // [2] value CTA: O rescaled, P buffer b ready for the MMA
+    B_PVDONE = B_PREADY + 2,         // [2] value CTA: PV of the page that used P buffer b complete
+    B_OFREE = B_PVDONE + 2,          // value CTA: O drained
+    B_DONE = B_OFREE + 1,            // MMA drain at exit
+    B_QREADY = B_DONE + 1,           // score CTA: the segment's query is in TMEM (4 softmax warps)
+    B_RFULL = B_QREADY + 1,          // MX caches: [RAW_STAGES] raw half page landed
+    B_REMPTY = B_RFULL + MAX_RAW,    // MX caches: [RAW_STAGES] the 4 converter warps read it
+    NBARS = B_REMPTY + MAX_RAW
 };
-constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-constexpr int OFF_RED = OFF_MISC + 16;            // schedule scratch (SCHED_SCRATCH words)
-constexpr int SMEM_BYTES = OFF_RED + SCHED_SCRATCH * 8;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// Shared-memory layout per cache format (KVF: KV_PLAIN, KV_MXFP8, KV_MXFP4).  Both CTAs of a
+// pair use the same offsets.  The plain cache streams bf16 pages by TMA into a 3-stage ring.
+// An MX cache streams raw half pages (codes, then the 32 rows' scale bytes) by bulk copy into
+// a raw ring; four converter warps widen them into a 2-stage bf16 ring of the same layout as
+// the TMA writes, so the MMA and softmax code is shared.
+template <int KVF>
+struct Lay {
+    static constexpr int STAGES = KVF == KV_PLAIN ? 3 : 2;
+    static constexpr int OFF_R = STAGES * V_STAGE_BYTES;           // value CTA: P buffers
+    static constexpr int ROW_BYTES = KVF == KV_MXFP4 ? WID / 2 : WID;  // code bytes per cache row
+    static constexpr int RAW_CODES = HALF * ROW_BYTES;
+    static constexpr int RAW_SCALES = HALF * (WID / MX_BLOCK);
+    static constexpr int RAW_STAGE = (RAW_CODES + RAW_SCALES + 127) & ~127;
+    static constexpr int RAW_STAGES = KVF == KV_MXFP4 ? 6 : (KVF == KV_MXFP8 ? 3 : 0);
+    static constexpr int RAW_RING = RAW_STAGES > 0 ? RAW_STAGES : 1;  // ring arithmetic (MX only)
+    static constexpr int RING_END = STAGES * S_STAGE_BYTES > OFF_R + R_BYTES ? STAGES * S_STAGE_BYTES
+                                                                             : OFF_R + R_BYTES;
+    static constexpr int OFF_RAW = RING_END;
+    static constexpr int OFF_BARS = OFF_RAW + RAW_STAGES * RAW_STAGE;
+    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+    static constexpr int OFF_RED = OFF_MISC + 16;                  // schedule scratch
+    static constexpr int SMEM_BYTES = OFF_RED + SCHED_SCRATCH * 8;
+    static constexpr int NTHREADS = KVF == KV_PLAIN ? 224 : 352;   // + 4 converter warps
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(RAW_STAGES <= MAX_RAW, "raw ring barriers");
+    static_assert(RAW_CODES % 16 == 0 && RAW_SCALES % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
 constexpr int TM_Q = 0, TM_S = 288, TM_O = 0;
-constexpr int NTHREADS = 224;
 constexpr float TAU = 8.0f;  // log2 units
 constexpr float LN2 = 0.6931471805599453f;
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 64, false, false);
@@ -136,14 +161,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
-__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + OFF_BARS + 8u * (uint32_t)i; }
+template <int KVF>
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
+    return base + Lay<KVF>::OFF_BARS + 8u * (uint32_t)i;
+}
 
 // ----------------------------------------------------------------------------- warp 0: TMA
-// Both CTAs run the same page sequence; the score CTA loads all nine 64-column chunks of a
-// page, the value CTA the eight latent chunks.
+// Both CTAs run the same page sequence.  Plain cache: the score CTA loads the segment's query
+// and then all nine 64-column chunks of each page, the value CTA the eight latent chunks, by
+// tensor TMA into the bf16 ring.  MX cache: both CTAs bulk-copy each page as two raw half pages
+// (32 rows of codes, then their scale bytes, both contiguous in the pool) into the raw ring; the
+// converter warps fill every item of the bf16 ring, the query's too (a parity wait on a ring
+// barrier is only unambiguous for a party that fills every item of the ring in order).
+template <int KVF>
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tm, const CUtensorMap* tmq, UnitCursor c,
                                          uint32_t base, uint32_t rank, const WaitCtl& wc) {
-    uint32_t g = 0;  // ring items issued
+    using L = Lay<KVF>;
+    constexpr int STAGES = L::STAGES;
+    uint32_t g = 0;       // plain cache: bf16 ring items (queries and pages), in ring order
+    uint32_t r = 0;       // MX cache: raw items issued
     bool ok = true;
     Segment sg;
     const int nch = rank == 0 ? 9 : LAT_CHUNKS;
@@ -160,11 +196,11 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             grid_dependency_wait();
             waited = true;
         }
-        if (rank == 0) {  // the segment's query: box b of the 18 is (columns 64*(b/2), rows 64*(b%2))
+        if (KVF == KV_PLAIN && rank == 0) {  // the segment's query: box b of the 18 is (columns 64*(b/2), rows 64*(b%2))
             for (int qi = 0; qi < Q_ITEMS; ++qi, ++g) {
                 const uint32_t stage = g % STAGES;
-                if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
-                const uint32_t fb = bar_addr(base, B_FULL + stage), dst = base + stage * S_STAGE_BYTES;
+                if (!wait_bar(bar_addr<KVF>(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
+                const uint32_t fb = bar_addr<KVF>(base, B_FULL + stage), dst = base + stage * S_STAGE_BYTES;
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)S_STAGE_BYTES);
                 for (int j = 0; j < 9; ++j) {
                     const int b = 9 * qi + j;
@@ -174,31 +210,183 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             if (!ok) break;
         }
         for (int pg = pg0; pg < sg.page_end; ++pg, ++g) {
-            const uint32_t stage = g % STAGES;
-            if (!wait_bar(bar_addr(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
             int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + pg);
             if (page < 0 || page >= a.num_pages) {
                 set_device_error(MLA_ERR_DEVICE_BOUNDS);
                 page = 0;  // keep the pipeline fed; the result of this query is void
             }
-            const uint32_t fb = bar_addr(base, B_FULL + stage);
-            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-            const uint32_t dst = base + stage * stage_bytes;
-            for (int cc = 0; cc < nch; ++cc) ptx::tma_load_2d(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
+            if (KVF == KV_PLAIN) {
+                const uint32_t stage = g % STAGES;
+                if (!wait_bar(bar_addr<KVF>(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
+                const uint32_t fb = bar_addr<KVF>(base, B_FULL + stage);
+                ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+                const uint32_t dst = base + stage * stage_bytes;
+                for (int cc = 0; cc < nch; ++cc) ptx::tma_load_2d(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
+            } else {
+                for (int hf = 0; hf < 2; ++hf, ++r) {
+                    const uint32_t rs = r % L::RAW_RING;
+                    if (!wait_bar(bar_addr<KVF>(base, B_REMPTY + rs), ((r / L::RAW_RING) & 1u) ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_addr<KVF>(base, B_RFULL + rs);
+                    const uint32_t dst = base + L::OFF_RAW + rs * L::RAW_STAGE;
+                    const long long row0 = (long long)page * PAGE + hf * HALF;
+                    ptx::mbar_arrive_expect_tx(fb, (uint32_t)(L::RAW_CODES + L::RAW_SCALES));
+                    ptx::bulk_load(dst, reinterpret_cast<const uint8_t*>(a.pool) + row0 * L::ROW_BYTES,
+                                   (uint32_t)L::RAW_CODES, fb);
+                    ptx::bulk_load(dst + L::RAW_CODES, reinterpret_cast<const uint8_t*>(a.scales) + row0 * (WID / MX_BLOCK),
+                                   (uint32_t)L::RAW_SCALES, fb);
+                }
+                if (!ok) break;
+            }
         }
     }
     if (!ok) {  // let loads already in flight land before the CTA leaves
         WaitCtl w2 = wc;
         w2.ignore_abort = true;
         w2.limit_ns = 20000000ull;
-        for (uint32_t k = g > (uint32_t)STAGES ? g - STAGES : 0u; k < g; ++k)
-            wait_bar(bar_addr(base, B_FULL + k % STAGES), (k / STAGES) & 1u, w2);
+        if (KVF == KV_PLAIN) {
+            for (uint32_t k = g > (uint32_t)STAGES ? g - STAGES : 0u; k < g; ++k)
+                wait_bar(bar_addr<KVF>(base, B_FULL + k % STAGES), (k / STAGES) & 1u, w2);
+        } else {
+            for (uint32_t k = r > (uint32_t)L::RAW_RING ? r - L::RAW_RING : 0u; k < r; ++k)
+                wait_bar(bar_addr<KVF>(base, B_RFULL + k % L::RAW_RING), (k / L::RAW_RING) & 1u, w2);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- MX converters
+// Warps 7-10 of both CTAs (MX caches only) fill every item of the bf16 ring, in order, each
+// warp waiting for the item's stage to be free and arriving on its full barrier (count 4).
+// Score CTA, the segment's query: warp 7 loads its two items by tensor TMA (the same 18 boxes
+// as a plain cache), completing their bytes on the full barrier.  Every page: the warps widen
+// its two raw half pages into the stage.  Item = (row, 16-byte group of
+// codes): an MXFP8 group is 16 codes of half a block, an MXFP4 group 32 codes of one block.
+// Each code becomes code value * 2^(scale byte - 127) in bf16, exactly, written at the place the
+// 128-byte-swizzled TMA layout gives it (64-column chunk, row, 16-byte piece p at
+// (p ^ (row & 7)) * 16).  Rows past the sequence end are written as zeros, so that whatever
+// bytes the pool holds there meet a zero weight as zeros.  The score CTA converts all 576
+// columns, the value CTA the 512 latent ones.
+template <int KVF>
+__device__ __forceinline__ void converter(const AttnArgs& a, const CUtensorMap* tmq, UnitCursor c, uint32_t base,
+                                          uint32_t rank, int cw, int lane, const WaitCtl& wc) {
+    using L = Lay<KVF>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int GC = KVF == KV_MXFP4 ? 32 : 16;   // codes per 16-byte group
+    constexpr int NW = GC / 2;                      // bf16 pairs per group
+    constexpr int SB = WID / MX_BLOCK;              // scale bytes per row
+    const int G = (rank == 0 ? WID : DC) / GC;      // groups of a row this CTA converts
+    const int n_items = HALF * G;
+    const int ctid = cw * 32 + lane;
+    const uint32_t stage_bytes = rank == 0 ? S_STAGE_BYTES : V_STAGE_BYTES;
+    uint32_t k = 0, r = 0;  // bf16 ring items, raw items
+    uint32_t q_end = 0;     // warp 7: one past the last query item loaded
+    bool ok = true, waited = false;
+    Segment sg;
+    while (ok && c.next(a.qs, &sg)) {
+        if (rank == 0) {
+            if (cw == 0 && lane == 0 && !waited) {
+                grid_dependency_wait();  // the query comes from the kernel before this one
+                waited = true;
+            }
+            for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) {
+                const uint32_t stage = k % STAGES;
+                if (!warp_wait(bar_addr<KVF>(base, B_EMPTY + stage), ((k / STAGES) & 1u) ^ 1u, wc, false, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_addr<KVF>(base, B_FULL + stage);
+                if (lane == 0) {
+                    if (cw == 0) {  // box b of the 18 is (columns 64*(b/2), rows 64*(b%2))
+                        const uint32_t dst = base + stage * S_STAGE_BYTES;
+                        ptx::mbar_arrive_expect_tx(fb, (uint32_t)S_STAGE_BYTES);
+                        for (int j = 0; j < 9; ++j) {
+                            const int b = 9 * qi + j;
+                            ptx::tma_load_2d(dst + j * CHUNK, tmq, (b >> 1) * 64, sg.q * NH + (b & 1) * 64, fb);
+                        }
+                        q_end = k + 1;
+                    } else {
+                        ptx::mbar_arrive(fb);
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++k) {
+            const uint32_t stage = k % STAGES;
+            if (!warp_wait(bar_addr<KVF>(base, B_EMPTY + stage), ((k / STAGES) & 1u) ^ 1u, wc, false, lane)) {
+                ok = false;
+                break;
+            }
+            const uint32_t dst = base + stage * stage_bytes;
+            const int valid = sg.len - pg * PAGE;  // rows of this page that hold tokens
+            for (int hf = 0; hf < 2; ++hf, ++r) {
+                const uint32_t rs = r % L::RAW_RING;
+                if (!warp_wait(bar_addr<KVF>(base, B_RFULL + rs), (r / L::RAW_RING) & 1u, wc, false, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t raw = base + L::OFF_RAW + rs * L::RAW_STAGE;
+#pragma unroll 1
+                for (int i = ctid; i < n_items; i += 128) {
+                    const int row = i / G, grp = i - row * G;
+                    const int trow = hf * HALF + row;
+                    const uint4 cv = ptx::ld_shared_v4u(raw + (uint32_t)(row * L::ROW_BYTES + grp * 16));
+                    const int blk = KVF == KV_MXFP4 ? grp : (grp >> 1);
+                    const float sc = exp2_int((int)ptx::ld_shared_u8(raw + (uint32_t)(L::RAW_CODES + row * SB + blk)) - 127);
+                    const uint32_t cw4[4] = {cv.x, cv.y, cv.z, cv.w};
+                    uint32_t w[NW];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (KVF == KV_MXFP8) {
+                            const float2 lo = e4m3x2_to_f32(cw4[j] & 0xFFFFu), hi = e4m3x2_to_f32(cw4[j] >> 16);
+                            w[2 * j] = ptx::pack_bf16(lo.x * sc, lo.y * sc);
+                            w[2 * j + 1] = ptx::pack_bf16(hi.x * sc, hi.y * sc);
+                        } else {
+#pragma unroll
+                            for (int bb = 0; bb < 4; ++bb) {
+                                const float2 v = e2m1x2_to_f32(cw4[j] >> (8 * bb));
+                                w[4 * j + bb] = ptx::pack_bf16(v.x * sc, v.y * sc);
+                            }
+                        }
+                    }
+                    if (trow >= valid) {
+#pragma unroll
+                        for (int q = 0; q < NW; ++q) w[q] = 0u;
+                    }
+                    // GC codes = GC bf16 = GC / 8 pieces of 16 bytes, starting at column grp * GC
+                    const int cc = (grp * GC) >> 6, p0 = ((grp * GC) & 63) >> 3;
+                    const uint32_t rowp = dst + (uint32_t)(cc * CHUNK + trow * 128);
+#pragma unroll
+                    for (int q = 0; q < GC / 8; ++q)
+                        ptx::st_shared_v4(rowp + ((uint32_t)((p0 + q) ^ (trow & 7)) << 4), w[4 * q], w[4 * q + 1],
+                                          w[4 * q + 2], w[4 * q + 3]);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_REMPTY + rs));
+            }
+            if (!ok) break;
+            ptx::fence_proxy_async();  // the tensor core reads the stage through the async proxy
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_FULL + stage));
+        }
+    }
+    if (!ok && cw == 0 && lane == 0) {  // let query loads still in flight land (bounded)
+        WaitCtl w2 = wc;
+        w2.ignore_abort = true;
+        w2.limit_ns = 20000000ull;
+        for (uint32_t q = q_end > (uint32_t)Q_ITEMS ? q_end - Q_ITEMS : 0u; q < q_end; ++q)
+            wait_bar(bar_addr<KVF>(base, B_FULL + q % STAGES), (q / STAGES) & 1u, w2);
     }
 }
 
 // ----------------------------------------------------------------------------- score CTA
+template <int KVF>
 __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
                                           const WaitCtl& wc) {
+    constexpr int STAGES = Lay<KVF>::STAGES;
     uint32_t g = 0, k = 0, segn = 0;  // pages, ring items, segments
     bool ok = true;
     Segment sg;
@@ -206,14 +394,14 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
         // the softmax warps put the segment's query into TMEM columns [TM_Q, TM_Q + 288) (they
         // do so only after reading the previous segment's last scores, i.e. after its QKs);
         // then the three ring stages that carried it are free
-        if (!wait_bar(bar_addr(base, B_QREADY), segn & 1u, wc)) break;
+        if (!wait_bar(bar_addr<KVF>(base, B_QREADY), segn & 1u, wc)) break;
         ptx::tc_fence_after();
-        for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) ptx::mbar_arrive(bar_addr(base, B_EMPTY + k % STAGES));
+        for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) ptx::mbar_arrive(bar_addr<KVF>(base, B_EMPTY + k % STAGES));
         ++segn;
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
             const uint32_t stage = k % STAGES, sb = g & 1u;
-            if (!wait_bar(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
-            if (!wait_bar(bar_addr(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
+            if (!wait_bar(bar_addr<KVF>(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
+            if (!wait_bar(bar_addr<KVF>(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
             ptx::tc_fence_after();
             // descriptors are the stage's base descriptor plus compile-time offsets (the 14-bit
             // address field cannot carry: shared addresses are < 256 KB).  The 36 MMAs are fully
@@ -228,28 +416,31 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
                     ptx::mma_ts(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
                                 IDESC_QK, (cc | kk) ? 1u : 0u);
             }
-            ptx::tc_commit(bar_addr(base, B_SFULL + sb));
-            ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
+            ptx::tc_commit(bar_addr<KVF>(base, B_SFULL + sb));
+            ptx::tc_commit(bar_addr<KVF>(base, B_EMPTY + stage));
         }
     }
     // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
     // whatever the configured limit (which may be microseconds when a caller tests timeouts)
-    ptx::tc_commit(bar_addr(base, B_DONE));
+    ptx::tc_commit(bar_addr<KVF>(base, B_DONE));
     WaitCtl w2 = wc;
     w2.ignore_abort = true;
     w2.limit_ns = 20000000ull;
-    wait_bar(bar_addr(base, B_DONE), 0, w2);
+    wait_bar(bar_addr<KVF>(base, B_DONE), 0, w2);
 }
 
+template <int KVF>
 __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, uint32_t base, uint32_t tmem,
                                               uint32_t peer, int warp, int lane, const WaitCtl& wc) {
+    constexpr int STAGES = Lay<KVF>::STAGES;
+    constexpr int OFF_R = Lay<KVF>::OFF_R;
     const AttnArgs& a = args.a;
     const int qd = warp & 3;  // TMEM lane quarter this warp may access
     const int h = qd * 32 + lane;
     const uint32_t lb = (uint32_t)(qd * 32) << 16;
     const uint32_t tS = tmem + lb + TM_S, tQ = tmem + lb + TM_Q;
     const uint32_t pbuf_r = ptx::mapa(base + OFF_R, peer);          // value CTA's P buffers
-    const uint32_t pfull_r = ptx::mapa(bar_addr(base, B_PFULL), peer);
+    const uint32_t pfull_r = ptx::mapa(bar_addr<KVF>(base, B_PFULL), peer);
     const uint32_t sw = (uint32_t)(h & 7);
     uint32_t g = 0, k = 0;  // pages, ring items
     bool ok = true;
@@ -260,7 +451,7 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
         // 2c + h/64, i.e. 32 columns of bf16 pairs
         for (int qi = 0; qi < Q_ITEMS && ok; ++qi, ++k) {
             const uint32_t stage = k % STAGES;
-            if (!warp_wait(bar_addr(base, B_FULL + stage), (k / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_FULL + stage), (k / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
 #pragma unroll 1
             for (int j = 0; j < 9; ++j) {
                 const int b = 9 * qi + j;
@@ -282,11 +473,11 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_QREADY));
+        if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_QREADY));
         float m_run = -INFINITY, l = 0.f;
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
             const uint32_t sb = g & 1u, use = g >> 1;
-            if (!warp_wait(bar_addr(base, B_SFULL + sb), use & 1u, wc, false, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_SFULL + sb), use & 1u, wc, false, lane)) { ok = false; break; }
             ptx::tc_fence_after();
             float s[64];
             {
@@ -303,7 +494,7 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_SFREE + sb));
+            if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_SFREE + sb));
 
             // scaled scores in log2 units; tokens past the sequence end are masked
             const int valid = sg.len - pg * PAGE;
@@ -331,7 +522,7 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             l += sum;
             // P row h -> value CTA, 128-byte swizzled (16-byte chunk k at k ^ (h & 7))
             const uint32_t pb = g & 1u;
-            if (!warp_wait(bar_addr(base, B_PEMPTY + pb), (use & 1u) ^ 1u, wc, true, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_PEMPTY + pb), (use & 1u) ^ 1u, wc, true, lane)) { ok = false; break; }
             const uint32_t row = pbuf_r + pb * PBUF_BYTES + (uint32_t)h * 128u;
             const uint32_t fb = pfull_r + 8u * pb;
 #pragma unroll
@@ -347,8 +538,11 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
 }
 
 // ----------------------------------------------------------------------------- value CTA
+template <int KVF>
 __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
                                           const WaitCtl& wc) {
+    constexpr int STAGES = Lay<KVF>::STAGES;
+    constexpr int OFF_R = Lay<KVF>::OFF_R;
     uint32_t g = 0, segn = 0;
     bool ok = true;
     Segment sg;
@@ -356,9 +550,9 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const bool first = pg == sg.page_begin;
             const uint32_t stage = g % STAGES, pb = g & 1u;
-            if (!wait_bar(bar_addr(base, B_FULL + stage), (g / STAGES) & 1u, wc)) { ok = false; break; }
-            if (!wait_bar(bar_addr(base, B_PREADY + pb), (g >> 1) & 1u, wc)) { ok = false; break; }
-            if (first && segn > 0 && !wait_bar(bar_addr(base, B_OFREE), (segn - 1) & 1u, wc)) { ok = false; break; }
+            if (!wait_bar(bar_addr<KVF>(base, B_FULL + stage), (g / STAGES) & 1u, wc)) { ok = false; break; }
+            if (!wait_bar(bar_addr<KVF>(base, B_PREADY + pb), (g >> 1) & 1u, wc)) { ok = false; break; }
+            if (first && segn > 0 && !wait_bar(bar_addr<KVF>(base, B_OFREE), (segn - 1) & 1u, wc)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint64_t da = ptx::desc_sw128(base + OFF_R + pb * PBUF_BYTES, 16, 1024);
             const uint64_t db = ptx::desc_sw128(base + stage * V_STAGE_BYTES, CHUNK, 1024);
@@ -370,22 +564,24 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
                                 db + (uint64_t)((hf * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV,
                                 (first && kk == 0) ? 0u : 1u);
             }
-            ptx::tc_commit(bar_addr(base, B_PVDONE + pb));
-            ptx::tc_commit(bar_addr(base, B_EMPTY + stage));
+            ptx::tc_commit(bar_addr<KVF>(base, B_PVDONE + pb));
+            ptx::tc_commit(bar_addr<KVF>(base, B_EMPTY + stage));
         }
         ++segn;
     }
     // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
     // whatever the configured limit (which may be microseconds when a caller tests timeouts)
-    ptx::tc_commit(bar_addr(base, B_DONE));
+    ptx::tc_commit(bar_addr<KVF>(base, B_DONE));
     WaitCtl w2 = wc;
     w2.ignore_abort = true;
     w2.limit_ns = 20000000ull;
-    wait_bar(bar_addr(base, B_DONE), 0, w2);
+    wait_bar(bar_addr<KVF>(base, B_DONE), 0, w2);
 }
 
+template <int KVF>
 __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem, int warp,
                                             int lane, const WaitCtl& wc) {
+    constexpr int OFF_R = Lay<KVF>::OFF_R;
     const int qd = warp & 3;
     const int h = qd * 32 + lane;
     const uint32_t tO = tmem + ((uint32_t)(qd * 32) << 16) + TM_O;
@@ -397,8 +593,8 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const bool first = pg == sg.page_begin;
             const uint32_t pb = g & 1u, use = g >> 1;
-            if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(bar_addr(base, B_PFULL + pb), PBUF_BYTES);
-            if (!warp_wait(bar_addr(base, B_PFULL + pb), use & 1u, wc, true, lane)) { ok = false; break; }
+            if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(bar_addr<KVF>(base, B_PFULL + pb), PBUF_BYTES);
+            if (!warp_wait(bar_addr<KVF>(base, B_PFULL + pb), use & 1u, wc, true, lane)) { ok = false; break; }
             const float2 meta = ptx::ld_shared_v2(base + OFF_R + pb * PBUF_BYTES + P_BYTES + (uint32_t)h * 8u);
             l_last = meta.y;
             const bool resc = !first && meta.x != 1.f;
@@ -406,7 +602,7 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
                 // O must be stable: the previous page's PV has completed.  pvdone is kept per P
                 // buffer so that no parity wait here is ever two phases away from its target.
                 const uint32_t gp = g - 1;
-                if (!warp_wait(bar_addr(base, B_PVDONE + (gp & 1u)), (gp >> 1) & 1u, wc, false, lane)) {
+                if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + (gp & 1u)), (gp >> 1) & 1u, wc, false, lane)) {
                     ok = false;
                     break;
                 }
@@ -432,13 +628,13 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
             ptx::fence_proxy_async();  // P arrived through the generic proxy; the MMA reads it via the async proxy
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_PREADY + pb));
+            if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_PREADY + pb));
         }
         if (!ok) break;
         // drain O / l once the segment's last PV has completed
         {
             const uint32_t gl = g - 1;
-            if (!warp_wait(bar_addr(base, B_PVDONE + (gl & 1u)), (gl >> 1) & 1u, wc, false, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + (gl & 1u)), (gl >> 1) & 1u, wc, false, lane)) { ok = false; break; }
         }
         ptx::tc_fence_after();
         const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
@@ -484,29 +680,32 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_addr(base, B_OFREE));
+        if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_OFREE));
     }
 }
 
 // Value CTA, warp 6: as soon as the PV of page g has completed (its P buffer is read), tell the
 // score CTA that the buffer may be refilled.  A warp of its own, so that the signal waits for
 // nothing but that PV.
+template <int KVF>
 __device__ __forceinline__ void value_release(const AttnArgs& a, UnitCursor c, uint32_t base, int lane,
                                               const WaitCtl& wc) {
-    const uint32_t pempty_r = ptx::mapa(bar_addr(base, B_PEMPTY), 0);  // the score CTA's barriers
+    const uint32_t pempty_r = ptx::mapa(bar_addr<KVF>(base, B_PEMPTY), 0);  // the score CTA's barriers
     uint32_t g = 0;
     Segment sg;
     while (c.next(a.qs, &sg)) {
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
-            if (!warp_wait(bar_addr(base, B_PVDONE + (g & 1u)), (g >> 1) & 1u, wc, false, lane)) return;
+            if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + (g & 1u)), (g >> 1) & 1u, wc, false, lane)) return;
             if (lane == 0) ptx::mbar_arrive_remote(pempty_r + 8u * (g & 1u));
         }
     }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+template <int KVF>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 1)
     tc_attention_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmq,
                         const TcArgs args) {
+    using L = Lay<KVF>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const AttnArgs& a = args.a;
     const uint32_t base = ptx::smem_u32(smem);
@@ -514,9 +713,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (threadIdx.x == 0) set_device_error(MLA_ERR_UNSUPPORTED);
         return;
     }
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-    long long* red = reinterpret_cast<long long*>(smem + OFF_RED);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    long long* red = reinterpret_cast<long long*>(smem + L::OFF_RED);
 
     // the split combine (a programmatic dependent) may be scheduled now; it waits for this
     // grid's completion before it reads anything this kernel writes
@@ -527,21 +726,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar_addr(base, B_FULL + s), 1);
-            ptx::mbar_init(bar_addr(base, B_EMPTY + s), 1);
+        for (int s = 0; s < L::STAGES; ++s) {
+            // MX caches: the four converter warps complete every stage (a query stage also
+            // waits for the TMA's bytes)
+            ptx::mbar_init(bar_addr<KVF>(base, B_FULL + s), KVF == KV_PLAIN ? 1 : 4);
+            ptx::mbar_init(bar_addr<KVF>(base, B_EMPTY + s), 1);
+        }
+        for (int s = 0; s < L::RAW_STAGES; ++s) {
+            ptx::mbar_init(bar_addr<KVF>(base, B_RFULL + s), 1);
+            ptx::mbar_init(bar_addr<KVF>(base, B_REMPTY + s), 4);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bar_addr(base, B_SFULL + b), 1);
-            ptx::mbar_init(bar_addr(base, B_SFREE + b), 4);
-            ptx::mbar_init(bar_addr(base, B_PFULL + b), 1);
-            ptx::mbar_init(bar_addr(base, B_PEMPTY + b), 1);
-            ptx::mbar_init(bar_addr(base, B_PREADY + b), 4);
-            ptx::mbar_init(bar_addr(base, B_PVDONE + b), 1);
+            ptx::mbar_init(bar_addr<KVF>(base, B_SFULL + b), 1);
+            ptx::mbar_init(bar_addr<KVF>(base, B_SFREE + b), 4);
+            ptx::mbar_init(bar_addr<KVF>(base, B_PFULL + b), 1);
+            ptx::mbar_init(bar_addr<KVF>(base, B_PEMPTY + b), 1);
+            ptx::mbar_init(bar_addr<KVF>(base, B_PREADY + b), 4);
+            ptx::mbar_init(bar_addr<KVF>(base, B_PVDONE + b), 1);
         }
-        ptx::mbar_init(bar_addr(base, B_OFREE), 4);
-        ptx::mbar_init(bar_addr(base, B_DONE), 1);
-        ptx::mbar_init(bar_addr(base, B_QREADY), 4);
+        ptx::mbar_init(bar_addr<KVF>(base, B_OFREE), 4);
+        ptx::mbar_init(bar_addr<KVF>(base, B_DONE), 1);
+        ptx::mbar_init(bar_addr<KVF>(base, B_QREADY), 4);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -550,7 +755,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         ptx::prefetch_tmap(&tmq);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(base + OFF_MISC, 512);
+        ptx::tmem_alloc(base + L::OFF_MISC, 512);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -569,18 +774,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const WaitCtl wc{args.wait_ns, abort_flag, false};
 
     if (warp == 0) {
-        if (lane == 0) producer(a, &tmap, &tmq, cur, base, rank, wc);
+        if (lane == 0) producer<KVF>(a, &tmap, &tmq, cur, base, rank, wc);
     } else if (warp == 1) {
         if (lane == 0) {
-            if (rank == 0) score_mma(a, cur, base, tmem, wc);
-            else value_mma(a, cur, base, tmem, wc);
+            if (rank == 0) score_mma<KVF>(a, cur, base, tmem, wc);
+            else value_mma<KVF>(a, cur, base, tmem, wc);
         }
     } else if (warp == 6) {
-        if (rank == 1) value_release(a, cur, base, lane, wc);
+        if (rank == 1) value_release<KVF>(a, cur, base, lane, wc);
+    } else if (warp >= 7) {
+        if (KVF != KV_PLAIN) converter<KVF>(a, &tmq, cur, base, rank, warp - 7, lane, wc);
     } else if (rank == 0) {
-        score_softmax(args, cur, base, tmem, peer, warp, lane, wc);
+        score_softmax<KVF>(args, cur, base, tmem, peer, warp, lane, wc);
     } else {
-        value_warps(a, cur, base, tmem, warp, lane, wc);
+        value_warps<KVF>(a, cur, base, tmem, warp, lane, wc);
     }
     // every CTA waits for the preceding grid before it leaves, even one without work: this
     // grid's completion then implies that grid's, which the combine after it relies on
@@ -634,35 +841,51 @@ inline bool tc_attention_supported(const mla_config* c, const mla_cache* k, int 
            c->page_size == tca::PAGE && cc_major == 10 && cc_minor == 3 && k->num_pages * tca::PAGE < (1LL << 31);
 }
 
-inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache, unsigned long long wait_ns,
-                                      bool pdl, cudaStream_t stream) {
+template <int KVF>
+inline mla_status tc_attention_launch_fmt(const AttnArgs& a, const mla_cache* cache, unsigned long long wait_ns,
+                                          bool pdl, cudaStream_t stream) {
+    using L = tca::Lay<KVF>;
     CUtensorMap tm, tmq;
-    if (!tca::encode_pool_map(&tm, cache->pool, cache->num_pages)) return MLA_ERR_CUDA;
     // the query rows viewed as [n_queries * 128, 576] bf16, box 64 columns x 64 rows
     if (!tca::encode_pool_map(&tmq, const_cast<void*>(a.q_cat), (long long)a.qs.n_queries * tca::NH / tca::PAGE))
         return MLA_ERR_CUDA;
+    if (KVF == KV_PLAIN) {
+        if (!tca::encode_pool_map(&tm, cache->pool, cache->num_pages)) return MLA_ERR_CUDA;
+    } else {
+        tm = tmq;  // unused: MX pages arrive by plain bulk copies
+    }
     tca::TcArgs t;
     t.a = a;
     t.wait_ns = wait_ns;
     t.scale_log2 = a.scale * 1.4426950408889634f;
-    if (cudaFuncSetAttribute(tca::tc_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tca::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(tca::tc_attention_kernel<KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM_BYTES) != cudaSuccess)
         return MLA_ERR_CUDA;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2 * a.n_units);
-    lc.blockDim = dim3(tca::NTHREADS);
-    lc.dynamicSmemBytes = tca::SMEM_BYTES;
+    lc.blockDim = dim3(L::NTHREADS);
+    lc.dynamicSmemBytes = L::SMEM_BYTES;
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = pdl ? 1 : 0;
-    if (cudaLaunchKernelEx(&lc, tca::tc_attention_kernel, tm, tmq, t) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&lc, tca::tc_attention_kernel<KVF>, tm, tmq, t) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
     }
     return MLA_OK;
+}
+
+inline mla_status tc_attention_launch(const AttnArgs& a, const mla_cache* cache, unsigned long long wait_ns,
+                                      bool pdl, cudaStream_t stream) {
+    switch (cache->kv_format) {
+        case MLA_KV_PLAIN: return tc_attention_launch_fmt<KV_PLAIN>(a, cache, wait_ns, pdl, stream);
+        case MLA_KV_MXFP8: return tc_attention_launch_fmt<KV_MXFP8>(a, cache, wait_ns, pdl, stream);
+        case MLA_KV_MXFP4: return tc_attention_launch_fmt<KV_MXFP4>(a, cache, wait_ns, pdl, stream);
+    }
+    return MLA_ERR_INVALID_ARG;
 }
 
 }  // namespace mla

@@ -23,6 +23,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "mx_format.cuh"
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -88,7 +89,22 @@ struct GemmArgs {
     const int* seq_idx;
     int max_pages, batch, page_size;
     long long num_pages;
+    int kv_format;      // APPEND: KV_PLAIN rows of bf16, or an MX cache (codes in pool)
+    void* scales;       // APPEND, MX cache: [num_pages, P, W / 32] scale bytes
 };
+
+// APPEND into an MX cache: the warp's 32 lanes hold one token's values of the block of 32
+// columns that starts at column cb (lane l: column cb + l) of cache row `ro` (ro < 0: a token
+// that goes nowhere; the warp still takes part in the shuffles).
+__device__ __forceinline__ void mx_append_block(const GemmArgs& g, int ro, int cb, float v, int lane) {
+    const int r = ro < 0 ? 0 : ro;
+    uint8_t* scale = reinterpret_cast<uint8_t*>(g.scales) + (size_t)r * (g.width / MX_BLOCK) + cb / MX_BLOCK;
+    if (g.kv_format == KV_MXFP8)
+        mx_store_block<KV_MXFP8>(reinterpret_cast<uint8_t*>(g.pool) + (size_t)r * g.width + cb, scale, v, lane, ro >= 0);
+    else
+        mx_store_block<KV_MXFP4>(reinterpret_cast<uint8_t*>(g.pool) + (size_t)r * (g.width / 2) + cb / 2, scale, v,
+                                 lane, ro >= 0);
+}
 
 // launch choices (0 = automatic), from the library's tuning knobs
 struct Tuning {
@@ -229,7 +245,21 @@ __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, co
         } else if (!rope_tile) {
             // latent columns: 16-byte stores of 8 columns (the row offset is per token, warp-uniform)
             const int ro = rowoff[nl];
-            store_cols8(out + (size_t)(ro < 0 ? 0 : ro) * g.width + mt * BM + tid, v, tid & 31, ro >= 0);
+            if (g.kv_format != KV_PLAIN)
+                mx_append_block(g, ro, mt * BM + (tid & ~31), v, tid & 31);
+            else
+                store_cols8(out + (size_t)(ro < 0 ? 0 : ro) * g.width + mt * BM + tid, v, tid & 31, ro >= 0);
+        } else if (g.kv_format != KV_PLAIN) {
+            // RoPE columns into an MX cache: every lane rotates its own element of the pair
+            // (2i, 2i+1) held by lanes tid, tid + 1; whole warps below d_r (a multiple of 32)
+            const float w = __shfl_xor_sync(0xffffffffu, v, 1);
+            if (tid < g.d_r) {
+                const int i = tid >> 1;
+                float cs, sn;
+                rope_cos_sin(__ldg(g.pos + n), g.rf.theta[i], &cs, &sn);
+                const float r = (tid & 1) ? w * sn + v * cs : v * cs - w * sn;
+                mx_append_block(g, rowoff[nl], g.d_c + (tid & ~31), r, tid & 31);
+            }
         } else {
             // the pair (2i, 2i+1) sits in lanes tid, tid + 1 of one warp
             const float w = __shfl_xor_sync(0xffffffffu, v, 1);
@@ -413,7 +443,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16);
             if (!rope_tile) {
                 // latent columns: per token, the 128 threads hold 128 consecutive values, stored
-                // 8 columns per 16-byte store
+                // 8 columns per 16-byte store (MX cache: one 32-column block per warp)
                 const int c = mt * BM + row;
                 for (int c0 = 0; c0 < g.n_pad; c0 += 32) {
                     uint32_t r[32];
@@ -423,7 +453,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int i = 0; i < 32; ++i) {
                         if (c0 + i >= n_here) break;  // warp-uniform
                         const int ro = rowoff[c0 + i];
-                        store_cols8(pool + (size_t)(ro < 0 ? 0 : ro) * g.width + c, __uint_as_float(r[i]), lane, ro >= 0);
+                        if (g.kv_format != KV_PLAIN)
+                            mx_append_block(g, ro, c - lane, __uint_as_float(r[i]), lane);
+                        else
+                            store_cols8(pool + (size_t)(ro < 0 ? 0 : ro) * g.width + c, __uint_as_float(r[i]), lane,
+                                        ro >= 0);
                     }
                 }
             } else {
@@ -441,7 +475,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                const int half = g.d_r / 2;
+                if (g.kv_format != KV_PLAIN) {
+                    // MX cache: warp w codes blocks (token, b) = items w, w + 4, ...; lane l
+                    // rotates element 32 b + l of the token's RoPE key
+                    const int nb = g.d_r / MX_BLOCK;
+                    for (int e = tid >> 5; e < n_here * nb; e += (NTHREADS - 64) / 32) {
+                        const int nl = e / nb, col = (e % nb) * MX_BLOCK + lane, i = col >> 1;
+                        float cs, sn;
+                        rope_cos_sin(__ldg(g.pos + n0 + nl), g.rf.theta[i], &cs, &sn);
+                        const float x0 = stg[nl * g.d_r + 2 * i], x1 = stg[nl * g.d_r + 2 * i + 1];
+                        const float v = (col & 1) ? x0 * sn + x1 * cs : x0 * cs - x1 * sn;
+                        mx_append_block(g, rowoff[nl], g.d_c + col - lane, v, lane);
+                    }
+                }
+                const int half = g.kv_format != KV_PLAIN ? 0 : g.d_r / 2;
                 for (int e = tid; e < n_here * half; e += NTHREADS - 64) {
                     const int nl = e / half, i = e % half;
                     if (rowoff[nl] < 0) continue;
@@ -702,6 +749,8 @@ inline mla_status tc_gemm_append(const mla_config* c, const mla_cache* k, const 
     g.batch = k->batch;
     g.page_size = c->page_size;
     g.num_pages = k->num_pages;
+    g.kv_format = k->kv_format;
+    g.scales = k->kv_scales;
     CUtensorMap ta, ta2, tb;
     if (!tcg::encode_2d(&ta, w_dkv, (uint64_t)c->d_latent, (uint64_t)c->d_model, (uint64_t)c->d_latent, 64) ||
         !tcg::encode_2d(&ta2, w_kr, (uint64_t)c->d_rope, (uint64_t)c->d_model, (uint64_t)c->d_rope, 64) ||

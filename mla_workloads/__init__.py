@@ -52,6 +52,7 @@ class Workload:
     tokens: int = 0       # query tokens (prefill / tiny)
     spare_pages: int = 64
     shuffled: bool = True
+    kv: str = ""          # "" plain cache rows of `dtype`; "mxfp8" / "mxfp4" an MX cache
 
     def describe(self) -> str:
         s = self.shape
@@ -72,6 +73,11 @@ WORKLOADS = {
     # Ragged high-concurrency decode with one appended token per sequence.
     "decode_ragged_b256": Workload("decode_ragged_b256", DEEPSEEK_V2, "bf16", "append_decode",
                                    seed=3, batch=256, len_range=(256, 8192)),
+    # The B=16 x 4096 decode over MX-encoded caches (E4M3 and E2M1 elements, 32-element blocks).
+    "decode_b16_l4096_mxfp8": Workload("decode_b16_l4096_mxfp8", DEEPSEEK_V2, "bf16", "decode", seed=5,
+                                       batch=16, lens=(4096,) * 16, kv="mxfp8"),
+    "decode_b16_l4096_mxfp4": Workload("decode_b16_l4096_mxfp4", DEEPSEEK_V2, "bf16", "decode", seed=6,
+                                       batch=16, lens=(4096,) * 16, kv="mxfp4"),
     # Causal prefill of 8192 tokens that also builds the cache.
     "prefill_t8192": Workload("prefill_t8192", DEEPSEEK_V2, "bf16", "prefill", seed=4, batch=1,
                               tokens=8192),
@@ -239,6 +245,73 @@ def make_decode_case(shape: Shape, dtype: str, lens, seed: int, *, spare_pages: 
     return case
 
 
+# MX caches (low-precision latent cache): synthetic codes and scale bytes, drawn directly.
+# E4M3 codes come from torch's float32 -> float8_e4m3fn cast of N(0,1) * 128 clipped to the
+# format's range (a storage cast, like the bf16 rounding above); E2M1 codes are uniform
+# nibbles; block scale bytes are uniform over a narrow band, so that the dequantised rows have
+# the spread of N(0,1) latents.  Slots that no token owns hold NaN codes (E4M3) or 0xFF bytes
+# and NaN scale bytes: an MX cache reader must never let them reach a result.
+MX_FMTS = {"mxfp8": 1, "mxfp4": 2}
+
+
+def mx_codes(rng, n_rows: int, width: int, fmt: str) -> np.ndarray:
+    if fmt == "mxfp8":
+        import torch
+        v = np.clip(normal(rng, (n_rows, width)) * np.float32(128.0), -448.0, 448.0).astype(np.float32)
+        return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return rng.integers(0, 256, size=(n_rows, width // 2), dtype=np.uint8)
+
+
+def mx_scale_bytes(rng, n_rows: int, width: int, fmt: str) -> np.ndarray:
+    lo, hi = (119, 121) if fmt == "mxfp8" else (125, 127)
+    return rng.integers(lo, hi, size=(n_rows, width // 32), endpoint=True).astype(np.uint8)
+
+
+def make_mx_decode_case(shape: Shape, fmt: str, lens, seed: int, *, spare_pages: int = 8,
+                        shuffled: bool = True, append: bool = False) -> dict:
+    """A decode problem over an MX-encoded paged cache (fmt "mxfp8" or "mxfp4").
+
+    Draw order (PCG64, `seed`): page table, then per sequence its codes and scale bytes, then
+    q_cat, q_nope, q_rope, W_UK, W_UV, W_O, then (append only) x, W_DKV, W_KR.  Queries and
+    weights are bf16 bits.
+    """
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int32)
+    B = int(lens.shape[0])
+    final = lens + (1 if append else 0)
+    pt, num_pages = make_page_table(rng, final, shape.page_size, spare_pages, shuffled)
+    W, ps = shape.width, shape.page_size
+    row_bytes = W if fmt == "mxfp8" else W // 2
+    codes = np.full((num_pages, ps, row_bytes), 0x7F if fmt == "mxfp8" else 0xFF, dtype=np.uint8)
+    scales = np.full((num_pages, ps, W // 32), 0xFF, dtype=np.uint8)
+    for b in range(B):
+        n = int(lens[b])
+        scatter_rows(codes, pt[b], mx_codes(rng, n, W, fmt))
+        scatter_rows(scales, pt[b], mx_scale_bytes(rng, n, W, fmt))
+    H, dc = shape.n_heads, shape.d_latent
+    qc = normal(rng, (B, H, W))
+    qc[..., :dc] *= np.float32(np.sqrt(shape.d_nope / dc))
+    case = dict(shape=shape, dtype="bf16", kv=fmt, codes=codes, scales=scales, page_table=pt,
+                num_pages=num_pages, seq_lens=final.astype(np.int32), pos=(final - 1).astype(np.int32),
+                q_cat=quantise(qc, "bf16"))
+    case.update(
+        q_nope=quantise(normal(rng, (B, H, shape.d_nope)), "bf16"),
+        q_rope=quantise(normal(rng, (B, H, shape.d_rope)), "bf16"),
+        w_uk=weight(rng, dc, H * shape.d_nope, "bf16"),
+        w_uv=weight(rng, dc, H * shape.d_nope, "bf16"),
+        w_o=weight(rng, H * shape.d_nope, shape.d_model, "bf16"),
+    )
+    if append:
+        case.update(
+            x=quantise(normal(rng, (B, shape.d_model)), "bf16"),
+            w_dkv=weight(rng, shape.d_model, dc, "bf16"),
+            w_kr=weight(rng, shape.d_model, shape.d_rope, "bf16"),
+            append_seq=np.arange(B, dtype=np.int32),
+            append_pos=lens.astype(np.int32),
+        )
+    return case
+
+
 def make_prefill_case(shape: Shape, dtype: str, T: int, seed: int, *, spare_pages: int = 8,
                       shuffled: bool = True) -> dict:
     """Causal prefill of one sequence of T tokens that first builds its cache from x.
@@ -301,6 +374,9 @@ def make_workload(name: str) -> dict:
                                  shuffled=w.shuffled)
     rng = np.random.default_rng(w.seed)
     lens = draw_lens(w, rng)
+    if w.kv:
+        return make_mx_decode_case(w.shape, w.kv, lens, w.seed + 1000, spare_pages=w.spare_pages,
+                                   shuffled=w.shuffled, append=(w.mode == "append_decode"))
     return make_decode_case(w.shape, w.dtype, lens, w.seed + 1000, spare_pages=w.spare_pages,
                             shuffled=w.shuffled, append=(w.mode == "append_decode"))
 

@@ -46,7 +46,7 @@ def test_nothing_else_is_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.mla_abi_version() == 1
+    assert lib.mla_abi_version() == 2
     for code in range(8):
         assert lib.mla_status_string(code)
     assert lib.mla_status_string(99) == b"unknown status"
@@ -96,6 +96,26 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.mla_query_proj(ctypes.byref(cfg), 16, 16, None, 16, 16, 1, None) == 1
     assert lib.mla_query_proj(ctypes.byref(cfg), 16, 16, 16, 16, 40, 1, None) == 1
     assert lib.mla_out_proj(ctypes.byref(cfg), 16, 16, 16, -1, None) == 1
+
+
+def test_mx_cache_checked_on_host(lib):
+    """An MX cache needs a known format, a 16-byte aligned scale array and rows of whole
+    32-element blocks; each failure is reported before anything touches a GPU."""
+    cfg = _cfg()
+    args = (5, 0, 1, 16, 16, 16, 16, 1 << 30, None)   # seq 5 >= batch 2: rejected last
+    ok = _lib.MlaCache(16, 10, 16, 4, 2, 16, _lib.MLA_KV_MXFP8, 32)
+    assert lib.mla_prefill(ctypes.byref(cfg), ctypes.byref(ok), *args) == 1
+    for fmt, scales, want in ((7, 32, 1), (_lib.MLA_KV_MXFP4, 0, 1), (_lib.MLA_KV_MXFP8, 40, 1)):
+        cache = _lib.MlaCache(16, 10, 16, 4, 2, 16, fmt, scales)
+        assert lib.mla_prefill(ctypes.byref(cfg), ctypes.byref(cache), 0, 0, 1, 16, 16, 16, 16, 1 << 30,
+                               None) == want
+    # W = 512 + 48 = 560 is not a multiple of 32
+    cfg = _cfg(d_rope=48)
+    assert lib.mla_prefill(ctypes.byref(cfg), ctypes.byref(ok), 0, 0, 1, 16, 16, 16, 16, 1 << 30, None) == 2
+    assert lib.mla_cache_append(ctypes.byref(cfg), ctypes.byref(ok), 16, 16, 16, 16, 16, 1, None) == 2
+    # a plain cache ignores kv_scales
+    plain = _lib.MlaCache(16, 10, 16, 4, 2, 16, _lib.MLA_KV_PLAIN, 0)
+    assert lib.mla_prefill(ctypes.byref(_cfg()), ctypes.byref(plain), *args) == 1
 
 
 def test_zero_tokens_is_a_noop(lib):
