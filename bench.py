@@ -58,7 +58,7 @@ def row_bytes(case) -> int:
     return s.width * 2
 
 
-def workload_numbers(case):
+def workload_numbers(case, form=""):
     """Algorithmic bytes and FLOPs of one attention launch (the split-attention kernel).
     Decode: cache rows read once (L*row_bytes: L*W*2 for bf16), queries (n_h*W*2), outputs (n_h*(d_c*2+4)) per
     sequence; FLOPs 2*L*n_h*(W + d_c) per sequence (scores plus weighted sum).
@@ -67,6 +67,13 @@ def workload_numbers(case):
     s = case["shape"]
     Wd = s.width
     per_q = s.n_heads * Wd * 2 + s.n_heads * (s.d_latent * 2 + 4)
+    if "T" in case and form == "unabsorbed":
+        # the flash kernel: query [T, n_h, d_h + d_r], K and V [T, n_h, d_h] and k_rope [T, d_r]
+        # read once, o [T, n_h, d_h] and lse written; 2 n_h (d_h + d_r + d_h) FLOPs per
+        # (query, visible key)
+        T, H, dh, dr = int(case["T"]), s.n_heads, s.d_nope, s.d_rope
+        bytes_ = T * H * (dh + dr) * 2 + 2 * T * H * dh * 2 + T * dr * 2 + T * H * (dh * 2 + 4)
+        return bytes_, H * (dh + dr + dh) * T * (T + 1)
     if "T" in case:
         T = int(case["T"])
         return T * Wd * 2 + T * per_q, s.n_heads * (Wd + s.d_latent) * T * (T + 1)
@@ -82,6 +89,7 @@ KERNEL_SOURCES = {
                      "mx_format.cuh"],
     "simt_attention": ["simt_attention.cuh", "sched.cuh", "mla_common.cuh", "mx_format.cuh"],
     "tc_gemm": ["tc_gemm.cuh", "tc_ptx.cuh", "mla_common.cuh", "mx_format.cuh"],
+    "tc_flash": ["tc_flash.cuh", "tc_ptx.cuh", "mla_common.cuh"],
 }
 
 
@@ -302,6 +310,9 @@ def config_of(name, case, out_proj=False):
                       "append_decode": "cache_append (one token per sequence) + absorb_q + decode + out",
                       "prefill": "cache_append (T tokens) + absorb_q + causal prefill + out"}[w.mode]
              + (" + out_proj (W_O)" if out_proj else "")}
+    if w.form == "unabsorbed":
+        extra["step"] = ("cache_append (T tokens) + un-absorbed causal prefill (gather, restore K and V, "
+                         "192-wide causal attention)" + (" + out_proj (W_O)" if out_proj else ""))
     if "T" in case:
         extra["query_tokens"] = int(case["T"])
     return {"workload": name, "batch": int(case["seq_lens"].shape[0]), **extra,
@@ -351,6 +362,7 @@ def run_ours(args):
         cache = M.PagedCache(dev(case["pool"]), i32(case["page_table"]), i32(case["seq_lens"]))
     q_nope, q_rope = dev(case["q_nope"]), dev(case["q_rope"])
     prefill = mode == "prefill"
+    unabsorbed = W.WORKLOADS[args.workload].form == "unabsorbed"
     pos = i32(case["append_pos"] if prefill else case["pos"])
     w_uk, w_uv = dev(case["w_uk"]), dev(case["w_uv"])
     w_o = dev(case["w_o"]) if args.out_proj else None
@@ -365,6 +377,11 @@ def run_ours(args):
     o = torch.empty((B, s.n_heads * s.d_nope), dtype=cfg.torch_dtype, device="cuda")
     out = torch.empty((B, s.d_model), dtype=cfg.torch_dtype, device="cuda") if args.out_proj else None
     ws = M.alloc_workspace(cfg)
+    if unabsorbed:
+        import ctypes
+        nb = ctypes.c_size_t(0)
+        M.lib().mla_prefill_unabsorbed_workspace_size(ctypes.byref(cfg.c()), 0, B, ctypes.byref(nb))
+        uws = torch.empty(int(nb.value), dtype=torch.uint8, device="cuda")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     flush_words = flush.view(torch.int64)
     stream = torch.cuda.current_stream()
@@ -379,6 +396,11 @@ def run_ours(args):
     def step(qn=q_nope, qr=q_rope, xx=None, oo=o, ll=lse, ff=out):
         if appending:  # the same positions every step: the cache ends each step identical
             M.mla_cache_append(cfg, cache, x if xx is None else xx, w_dkv, w_kr, a_seq, a_pos, stream=stream)
+        if unabsorbed:
+            M.mla_prefill_unabsorbed(cfg, cache, 0, 0, qn, qr, w_uk, w_uv, o=oo, lse=ll, workspace=uws, stream=stream)
+            if args.out_proj:
+                M.mla_out_proj(cfg, oo, w_o, out=ff, stream=stream)
+            return
         M.mla_absorb_q(cfg, qn, qr, pos, w_uk, q_cat=q_cat, stream=stream)
         if prefill:
             M.mla_prefill(cfg, cache, 0, 0, q_cat, o_lat=o_lat, lse=ll, workspace=ws, stream=stream)
@@ -479,12 +501,12 @@ def run_ours(args):
         dist.destroy_process_group()
         return 0
 
-    alg_bytes, alg_flops = workload_numbers(case)
+    alg_bytes, alg_flops = workload_numbers(case, W.WORKLOADS[args.workload].form)
     hbm, tflops, src = peaks()
     k_mean_s = (sum(kern_ms) / K) * 1e-3
     achieved = alg_bytes / k_mean_s / 1e9
     tensor_bound = alg_flops / (tflops * 1e12) > alg_bytes / (hbm * 1e9)
-    kernel_key = "tc_attention" if path == 2 else "simt_attention"
+    kernel_key = {2: "tc_attention", 3: "tc_flash"}.get(path, "simt_attention")
     line = {
         "metric": METRIC,
         "value": value,

@@ -214,6 +214,32 @@ MLA_API mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, in
                        int32_t q_start, int32_t n_queries, const void* q_cat, void* o_lat,
                        float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
+/* mla_prefill_unabsorbed - the prefill chain of [OPN] s.2 in its own form, not absorbed:
+ * "Restore K, V from c_kv" (K = c_kv @ W_UK, V = c_kv @ W_UV, every head), then standard
+ * causal attention with [GLO]'s decoupled RoPE key, for n_queries consecutive tokens of
+ * sequence `seq` (query i at position q_start + i, seeing tokens t <= q_start + i, which must
+ * already be in the cache):
+ *   s[i,h,t] = ([q_nope[i,h] | RoPE(q_rope[i,h], q_start+i)] . [K[t,h] | k_rope[t]]) * scale
+ *   lse[i,h] = log sum_t exp(s[i,h,t])
+ *   o[i, h*d_h:(h+1)*d_h] = sum_t exp(s[i,h,t] - lse[i,h]) * V[t,h]
+ * This is the same o as mla_prefill followed by mla_out, computed with fewer FLOPs for long
+ * prefills (restoring K and V costs 4 L d_c n_h d_h, the attention about 2 T^2 n_h (d_h+d_r)
+ * against 2 T^2 n_h (2 d_c + d_r) absorbed).  K, V and the query are rounded to bf16.
+ * q_nope device [n_queries, n_h, d_h]; q_rope device [n_queries, n_h, d_r] (not rotated);
+ * w_uk, w_uv device [d_c, n_h*d_h]; o device [n_queries, n_h*d_h]; lse device float
+ * [n_queries, n_h].  workspace: device, 256-byte aligned, at least
+ * mla_prefill_unabsorbed_workspace_size() bytes (the gathered cache rows, K, V and the rotated
+ * query; about 1 GB at L = T = 8192).  Needs cfg->dtype == MLA_BF16, d_nope == 128,
+ * d_rope == 64, d_latent a multiple of 64, a plain cache and sm_103 (else MLA_ERR_UNSUPPORTED).
+ * n_queries == 0 is a no-op. */
+MLA_API mla_status mla_prefill_unabsorbed_workspace_size(const mla_config* cfg, int32_t q_start,
+                                                         int32_t n_queries, size_t* bytes);
+MLA_API mla_status mla_prefill_unabsorbed(const mla_config* cfg, const mla_cache* cache, int32_t seq,
+                                          int32_t q_start, int32_t n_queries, const void* q_nope,
+                                          const void* q_rope, const void* w_uk, const void* w_uv,
+                                          void* o, float* lse, void* workspace,
+                                          size_t workspace_bytes, mla_stream_t stream);
+
 /* mla_out - absorbed output up-projection ([OPN] s.2 "V = c_kv @ W_UV", folded into the
  * output side as [GLO] describes):  o[n, h*d_h:(h+1)*d_h] = o_lat[n,h,:] @ W_UV[:, h*d_h:(h+1)*d_h]
  * o_lat device [n_tokens, n_h, d_c]; w_uv device [d_c, n_h*d_h]; o device [n_tokens, n_h*d_h].
@@ -256,17 +282,17 @@ typedef enum {
 } mla_tuning_key;
 MLA_API int32_t mla_set_tuning(int32_t key, int32_t value);
 
-/* Timing hook for benchmarks: when both are non-NULL, the next mla_decode / mla_prefill
- * calls on this thread record `before` (a cudaEvent_t) on their stream immediately before
- * the split-attention kernel and `after` immediately after it, so the caller can time that
- * kernel alone.  Pass NULLs to stop.  The events stay owned by the caller. */
+/* Timing hook for benchmarks: when both are non-NULL, the next mla_decode / mla_prefill /
+ * mla_prefill_unabsorbed calls on this thread record `before` (a cudaEvent_t) on their stream
+ * immediately before the attention kernel and `after` immediately after it, so the caller can
+ * time that kernel alone.  Pass NULLs to stop.  The events stay owned by the caller. */
 MLA_API void mla_set_attention_events(void* before, void* after);
 
 /* Number of CUDA kernels this process has launched through libmla so far. */
 MLA_API uint64_t mla_kernel_launches(void);
 
-/* Which kernel family the last mla_decode/mla_prefill call on this thread used:
- * 0 none yet, 1 SIMT, 2 tcgen05. */
+/* Which kernel family the last attention call on this thread used:
+ * 0 none yet, 1 SIMT, 2 tcgen05 (absorbed), 3 tcgen05 un-absorbed causal (mla_prefill_unabsorbed). */
 MLA_API int32_t mla_last_attention_path(void);
 
 #ifdef __cplusplus

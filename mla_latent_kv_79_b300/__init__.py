@@ -16,7 +16,8 @@ from . import _lib
 from ._lib import MLAError, MLA_F32, MLA_BF16, MLA_KV_PLAIN, MLA_KV_MXFP8, MLA_KV_MXFP4  # noqa: F401
 
 __all__ = ["MLAConfig", "PagedCache", "mla_cache_append", "mla_absorb_q", "mla_workspace_size",
-           "mla_decode", "mla_decode_static", "mla_prefill", "mla_out", "mla_out_proj", "mla_query_proj",
+           "mla_decode", "mla_decode_static", "mla_prefill", "mla_prefill_unabsorbed", "mla_out", "mla_out_proj",
+           "mla_query_proj",
            "mla_get_device_error",
            "mla_set_tuning",
            "mla_last_attention_path", "MLAError", "lib"]
@@ -155,6 +156,28 @@ def mla_prefill(cfg: MLAConfig, cache: PagedCache, seq: int, q_start: int, q_cat
                            _stream(stream))
     _lib.check(st, "mla_prefill")
     return o_lat, lse
+
+
+def mla_prefill_unabsorbed(cfg: MLAConfig, cache: PagedCache, seq: int, q_start: int, q_nope, q_rope, w_uk, w_uv,
+                           o=None, lse=None, workspace=None, stream=None):
+    """Causal prefill in the un-absorbed form (restore K and V, 192-wide scores); returns (o, lse)
+    with o [T, n_h * d_h], the output mla_prefill + mla_out would give."""
+    T = q_nope.shape[0]
+    dev = q_nope.device
+    if o is None:
+        o = torch.empty((T, cfg.n_heads * cfg.d_nope), dtype=cfg.torch_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T, cfg.n_heads), dtype=torch.float32, device=dev)
+    if workspace is None:
+        b = ctypes.c_size_t(0)
+        _lib.check(lib().mla_prefill_unabsorbed_workspace_size(ctypes.byref(cfg.c()), q_start, T, ctypes.byref(b)),
+                   "mla_prefill_unabsorbed_workspace_size")
+        workspace = torch.empty(int(b.value), dtype=torch.uint8, device=dev)
+    st = lib().mla_prefill_unabsorbed(ctypes.byref(cfg.c()), ctypes.byref(cache.c()), seq, q_start, T, _ptr(q_nope),
+                                      _ptr(q_rope), _ptr(w_uk), _ptr(w_uv), _ptr(o), _ptr(lse), _ptr(workspace),
+                                      workspace.numel(), _stream(stream))
+    _lib.check(st, "mla_prefill_unabsorbed")
+    return o, lse
 
 
 def mla_out(cfg: MLAConfig, o_lat, w_uv, o=None, stream=None):

@@ -49,6 +49,8 @@ SIGNATURES = {
     "mla_decode": (_I, [_CFG, _CACHE, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_decode_static": (_I, [_CFG, _CACHE, _P, _P, _P, _P]),
     "mla_prefill": (_I, [_CFG, _CACHE, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_prefill_unabsorbed_workspace_size": (_I, [_CFG, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    "mla_prefill_unabsorbed": (_I, [_CFG, _CACHE, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_out": (_I, [_CFG, _P, _P, _P, _I, _P]),
     "mla_out_proj": (_I, [_CFG, _P, _P, _P, _I, _P]),
     "mla_query_proj": (_I, [_CFG, _P, _P, _P, _P, _P, _I, _P]),

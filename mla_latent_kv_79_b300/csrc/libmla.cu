@@ -15,6 +15,7 @@
 #include "simt_attention.cuh"
 #include "tc_attention.cuh"
 #include "tc_gemm.cuh"
+#include "tc_flash.cuh"
 
 namespace mla {
 
@@ -51,7 +52,8 @@ static mla_status device_info(DeviceInfo** out) {
                 (const void*)tca::tc_attention_kernel<KV_PLAIN>, (const void*)tca::tc_attention_kernel<KV_MXFP8>,
                 (const void*)tca::tc_attention_kernel<KV_MXFP4>, (const void*)tcg::tc_gemm_kernel<tcg::ABSORB>,
                 (const void*)tcg::tc_gemm_kernel<tcg::OUT>, (const void*)tcg::tc_gemm_kernel<tcg::APPEND>,
-                (const void*)tcg::tc_gemm_kernel<tcg::OPROJ>};
+                (const void*)tcg::tc_gemm_kernel<tcg::OPROJ>, (const void*)tcf::prep_kernel,
+                (const void*)tcf::flash_kernel};
             for (const void* f : fns)
                 if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
@@ -445,6 +447,133 @@ mla_status mla_prefill(const mla_config* cfg, const mla_cache* cache, int32_t se
     qs.max_len = cache->max_pages * cfg->page_size;
     return attention(cfg, cache, qs, q_cat, o_lat, lse, workspace, workspace_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+static bool unabsorbed_supported(const mla_config* c, const mla_cache* k, const DeviceInfo* d) {
+    return c->dtype == MLA_BF16 && c->d_nope == tcf::DH && c->d_rope == tcf::DR && c->d_latent % 64 == 0 &&
+           d->cc_major == 10 && d->cc_minor == 3 && k->kv_format == MLA_KV_PLAIN;
+}
+
+mla_status mla_prefill_unabsorbed_workspace_size(const mla_config* cfg, int32_t q_start, int32_t n_queries,
+                                                  size_t* bytes) {
+    if (!bytes || q_start < 0 || n_queries < 0) return MLA_ERR_INVALID_ARG;
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    *bytes = tcf::unabsorbed_ws(cfg->n_heads, cfg->d_nope, cfg->d_rope, cfg->d_latent + cfg->d_rope,
+                                (long long)q_start + n_queries, n_queries).total;
+    return MLA_OK;
+}
+
+mla_status mla_prefill_unabsorbed(const mla_config* cfg, const mla_cache* cache, int32_t seq, int32_t q_start,
+                                  int32_t n_queries, const void* q_nope, const void* q_rope, const void* w_uk,
+                                  const void* w_uv, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                  mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if ((st = check_cache(cfg, cache)) != MLA_OK) return st;
+    if (seq < 0 || seq >= cache->batch || q_start < 0 || n_queries < 0) return MLA_ERR_INVALID_ARG;
+    if ((long long)q_start + n_queries > (long long)cache->max_pages * cfg->page_size) return MLA_ERR_INVALID_ARG;
+    if (n_queries == 0) return MLA_OK;
+    if (!q_nope || !q_rope || !w_uk || !w_uv || !o || !lse) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(o) ||
+        !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    if (!unabsorbed_supported(cfg, cache, dev) || (long long)cfg->n_heads * n_queries >= (1LL << 31))
+        return MLA_ERR_UNSUPPORTED;
+    const int W = cfg->d_latent + cfg->d_rope, n_h = cfg->n_heads;
+    const long long L = (long long)q_start + n_queries;
+    const tcf::UnabsorbedWs ws = tcf::unabsorbed_ws(n_h, cfg->d_nope, cfg->d_rope, W, L, n_queries);
+    if (!workspace || workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MLA_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* w8 = reinterpret_cast<uint8_t*>(workspace);
+    bf16* rows = reinterpret_cast<bf16*>(w8 + ws.rows);
+    bf16* K = reinterpret_cast<bf16*>(w8 + ws.k);
+    bf16* V = reinterpret_cast<bf16*>(w8 + ws.v);
+    bf16* qu = reinterpret_cast<bf16*>(w8 + ws.qu);
+    const bool pdl = g_tune[MLA_TUNE_NO_PDL].load() == 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+    // 1. gather the sequence's rows and build the un-absorbed query
+    tcf::PrepArgs p{};
+    p.pool = reinterpret_cast<const bf16*>(cache->pool);
+    p.page_row = cache->page_table + (size_t)seq * cache->max_pages;
+    p.max_pages = cache->max_pages;
+    p.num_pages = cache->num_pages;
+    p.page_size = cfg->page_size;
+    p.width = W;
+    p.n_keys = (int)L;
+    p.rows = rows;
+    p.q_nope = reinterpret_cast<const bf16*>(q_nope);
+    p.q_rope = reinterpret_cast<const bf16*>(q_rope);
+    p.n_queries = n_queries;
+    p.n_h = n_h;
+    p.q_start = q_start;
+    rope_freq_fill(&p.rf, cfg->d_rope, cfg->rope_base);
+    p.qu = qu;
+    const long long groups = L * (W / 8) + (long long)n_queries * n_h * ((tcf::DH + tcf::DR) / 8);
+    long long blocks = (groups + 255) / 256;
+    if (blocks > 8LL * max_units(dev)) blocks = 8LL * max_units(dev);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)blocks);
+    lc.blockDim = dim3(256);
+    lc.stream = s;
+    lc.attrs = attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&lc, tcf::prep_kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    count_launches(1);
+    // 2. K = c_kv . W_UK and V = c_kv . W_UV over the gathered rows (row pitch W)
+    const tcg::Tuning tu = gemm_tuning((unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull);
+    const long long hd = (long long)n_h * cfg->d_nope;
+    if ((st = tc_gemm_dense(cfg, rows, w_uk, K, cfg->d_latent, hd, (int)L, tu, s, W)) != MLA_OK) return st;
+    count_launches(1);
+    if ((st = tc_gemm_dense(cfg, rows, w_uv, V, cfg->d_latent, hd, (int)L, tu, s, W)) != MLA_OK) return st;
+    count_launches(1);
+    // 3. causal attention per (head, 128-query tile)
+    CUtensorMap tmq, tmk, tmr, tmv;
+    if (!tcf::encode_map(&tmq, qu, tcf::DQ, (uint64_t)n_h * n_queries, tcf::DQ) ||
+        !tcf::encode_map(&tmk, K, (uint64_t)hd, (uint64_t)L, (uint64_t)hd) ||
+        !tcf::encode_map(&tmr, rows, (uint64_t)W, (uint64_t)L, (uint64_t)W) ||
+        !tcf::encode_map(&tmv, V, (uint64_t)hd, (uint64_t)L, (uint64_t)hd))
+        return MLA_ERR_CUDA;
+    tcf::FlashArgs fa{};
+    fa.n_queries = n_queries;
+    fa.n_keys = (int)L;
+    fa.n_h = n_h;
+    fa.q_start = q_start;
+    fa.rope_col = cfg->d_latent;
+    fa.scale_log2 = scale_of(cfg) * 1.4426950408889634f;
+    fa.o = reinterpret_cast<bf16*>(o);
+    fa.lse = lse;
+    fa.wait_ns = (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull;
+    if (cudaFuncSetAttribute(tcf::flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcf::SMEM_BYTES) !=
+        cudaSuccess)
+        return MLA_ERR_CUDA;
+    const int n_qt = (n_queries + tcf::BQ - 1) / tcf::BQ;
+    cudaLaunchConfig_t lf = {};
+    lf.gridDim = dim3((unsigned)(n_qt * n_h));
+    lf.blockDim = dim3(tcf::NTHREADS);
+    lf.dynamicSmemBytes = tcf::SMEM_BYTES;
+    lf.stream = s;
+    lf.attrs = attr;
+    lf.numAttrs = pdl ? 1 : 0;
+    const bool timed = g_ev_before && g_ev_after;
+    if (timed) cudaEventRecord(g_ev_before, s);
+    if (cudaLaunchKernelEx(&lf, tcf::flash_kernel, tmq, tmk, tmr, tmv, fa) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+    }
+    if (timed) cudaEventRecord(g_ev_after, s);
+    count_launches(1);
+    g_last_path = 3;
+    return launch_status();
 }
 
 mla_status mla_out(const mla_config* cfg, const void* o_lat, const void* w_uv, void* o,

@@ -701,7 +701,8 @@ inline bool tc_gemm_dense_supported(const mla_config* c, long long K, long long 
 // can be larger than L2, so up to 256 tokens share one token tile and W is streamed once; K is
 // then split over clusters of 8 CTAs when the output tiles alone would leave SMs idle.
 inline mla_status tc_gemm_dense(const mla_config* c, const void* in, const void* w, void* out, long long K,
-                                long long M, int n, const tcg::Tuning& t, cudaStream_t stream) {
+                                long long M, int n, const tcg::Tuning& t, cudaStream_t stream,
+                                long long in_pitch = 0) {  // elements per input row (0: K)
     tcg::GemmArgs g{};
     g.mode = tcg::OPROJ;
     g.n_tokens = n;
@@ -713,7 +714,7 @@ inline mla_status tc_gemm_dense(const mla_config* c, const void* in, const void*
     g.out = out;
     CUtensorMap ta, tb;
     if (!tcg::encode_2d(&ta, w, (uint64_t)M, (uint64_t)K, (uint64_t)M, 64) ||
-        !tcg::encode_2d(&tb, in, (uint64_t)K, (uint64_t)n, (uint64_t)K, (uint32_t)g.n_pad))
+        !tcg::encode_2d(&tb, in, (uint64_t)K, (uint64_t)n, (uint64_t)(in_pitch > 0 ? in_pitch : K), (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
     return tcg::launch(g, ta, tb, ta, (int)(M / tcg::BM), 1, t, stream);
 }

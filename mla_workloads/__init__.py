@@ -53,6 +53,7 @@ class Workload:
     spare_pages: int = 64
     shuffled: bool = True
     kv: str = ""          # "" plain cache rows of `dtype`; "mxfp8" / "mxfp4" an MX cache
+    form: str = ""        # prefill: "" absorbed (the latent path), "unabsorbed" (restore K and V)
 
     def describe(self) -> str:
         s = self.shape
@@ -81,6 +82,9 @@ WORKLOADS = {
     # Causal prefill of 8192 tokens that also builds the cache.
     "prefill_t8192": Workload("prefill_t8192", DEEPSEEK_V2, "bf16", "prefill", seed=4, batch=1,
                               tokens=8192),
+    # The same prefill in the un-absorbed form of the operator notes (restore K and V per head).
+    "prefill_t8192_unabsorbed": Workload("prefill_t8192_unabsorbed", DEEPSEEK_V2, "bf16", "prefill", seed=4,
+                                         batch=1, tokens=8192, form="unabsorbed"),
 }
 
 

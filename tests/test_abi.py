@@ -118,6 +118,26 @@ def test_mx_cache_checked_on_host(lib):
     assert lib.mla_prefill(ctypes.byref(_cfg()), ctypes.byref(plain), *args) == 1
 
 
+def test_unabsorbed_prefill_checked_on_host(lib):
+    """Workspace size is the sum of its 256-byte-aligned parts; bad shapes, positions, pointers and
+    workspaces are rejected before anything touches a GPU."""
+    cfg = _cfg()
+    b = ctypes.c_size_t(0)
+    assert lib.mla_prefill_unabsorbed_workspace_size(ctypes.byref(cfg), 100, 28, ctypes.byref(b)) == 0
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    L, T = 128, 28
+    assert b.value == al(L * 576 * 2) + 2 * al(L * 128 * 128 * 2) + al(T * 128 * 192 * 2)
+    assert lib.mla_prefill_unabsorbed_workspace_size(ctypes.byref(cfg), -1, 28, ctypes.byref(b)) == 1
+    cache = _lib.MlaCache(16, 10, 16, 4, 2, 16, 0, 0)
+    args = lambda seq, q0, n: (ctypes.byref(cfg), ctypes.byref(cache), seq, q0, n, 16, 16, 16, 16, 16, 16,  # noqa: E731
+                               256, 1 << 30, None)
+    assert lib.mla_prefill_unabsorbed(*args(2, 0, 1)) == 1       # seq outside the batch
+    assert lib.mla_prefill_unabsorbed(*args(0, 250, 10)) == 1    # past the page table (4 pages of 64)
+    assert lib.mla_prefill_unabsorbed(*args(0, 0, 0)) == 0       # no queries: a no-op
+    bad = (ctypes.byref(cfg), ctypes.byref(cache), 0, 0, 1, 16, 16, 16, 24, 16, 16, 256, 1 << 30, None)
+    assert lib.mla_prefill_unabsorbed(*bad) == 1                 # misaligned w_uv
+
+
 def test_zero_tokens_is_a_noop(lib):
     cfg = _cfg()
     assert lib.mla_absorb_q(ctypes.byref(cfg), None, None, None, None, None, 0, None) == 0
