@@ -116,6 +116,33 @@ def query_projection(x, w_q, w_qr, pos, n_h: int, base: float):
     return q, rope_rotate(qr, np.asarray(pos)[:, None], base)
 
 
+def query_latent(x, w_dq):
+    """Compressed query ([OPN] s.4 'c_q = x @ W_DQ'): x [N, d_model], w_dq [d_model, d_cq]."""
+    return np.asarray(x, dtype=F64) @ np.asarray(w_dq, dtype=F64)
+
+
+def query_projection_compressed(x, w_dq, w_uq, w_qr, pos, n_h: int, base: float):
+    """The query side with compression ([OPN] s.4): c_q = x @ W_DQ, then Q = c_q @ W_UQ, and
+    the per-head RoPE query from the same latent, RoPE(c_q @ W_QR) (reading: with compression
+    the decoupled RoPE query is projected from c_q, as the uncompressed one is from x).
+
+    x [N, d_model], w_dq [d_model, d_cq], w_uq [d_cq, n_h*d_h], w_qr [d_cq, n_h*d_rope], pos [N].
+    Returns q_nope [N, n_h, d_h], q_rope [N, n_h, d_rope] (rotated).
+    """
+    return query_projection(query_latent(x, w_dq), w_uq, w_qr, pos, n_h, base)
+
+
+def absorb_uq_uk(w_uq, w_uk, n_h: int):
+    """W_UQ folded into W_UK ([GLO] absorption, [RMJ] associativity): per head the
+    [d_cq, d_c] product W_UQ_h @ W_UK_h^T, so that c_q @ (W_UQ_h @ W_UK_h^T) is the absorbed
+    query's latent part.  w_uq [d_cq, n_h*d_h], w_uk [d_c, n_h*d_h].  Returns [d_cq, n_h*d_c]
+    with head h in column block h."""
+    w_uq = np.asarray(w_uq, dtype=F64)
+    w_uk = np.asarray(w_uk, dtype=F64)
+    d_h = w_uq.shape[1] // n_h
+    return np.concatenate([head_cols(w_uq, h, d_h) @ head_cols(w_uk, h, d_h).T for h in range(n_h)], axis=1)
+
+
 def restore_kv(c_kv, w_uk, w_uv, n_h: int):
     """Up-projections that restore per-head K and V from the latent ([OPN] s.2
     'K = c_kv @ W_UK', 'V = c_kv @ W_UV').  Returns K, V as [L, n_h, d_h]."""

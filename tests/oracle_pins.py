@@ -131,6 +131,47 @@ def pin_query_projection_bruteforce(O):
             assert abs(qr[n, h, 1] - (a * math.sin(p) + b * math.cos(p))) < 1e-12
 
 
+def pin_compressed_query(O):
+    """c_q = x W_DQ by brute force; the compressed query equals the direct one with
+    W_Q = W_DQ W_UQ and W_QR = W_DQ W_QR' (associativity); with W_DQ = I it is the direct one."""
+    r = np.random.default_rng(17)
+    n_h, dh, dr, dm, dcq = 2, 3, 2, 5, 4
+    x = r.standard_normal((3, dm))
+    wdq = r.standard_normal((dm, dcq))
+    wuq, wqr = r.standard_normal((dcq, n_h * dh)), r.standard_normal((dcq, n_h * dr))
+    cq = O.query_latent(x, wdq)
+    for n in range(3):
+        for k in range(dcq):
+            assert abs(cq[n, k] - sum(x[n, i] * wdq[i, k] for i in range(dm))) < 1e-12
+    pos = np.array([0, 5, 1000])
+    qn, qr = O.query_projection_compressed(x, wdq, wuq, wqr, pos, n_h, 10000.0)
+    qn2, qr2 = O.query_projection(x, wdq @ wuq, wdq @ wqr, pos, n_h, 10000.0)
+    assert np.max(np.abs(qn - qn2)) < 1e-12 and np.max(np.abs(qr - qr2)) < 1e-12
+    qn3, qr3 = O.query_projection_compressed(cq, np.eye(dcq), wuq, wqr, pos, n_h, 10000.0)
+    assert np.max(np.abs(qn3 - qn)) < 1e-12 and np.max(np.abs(qr3 - qr)) < 1e-12
+    # the RoPE query comes from c_q (not from x): W_QR has d_cq rows
+    assert qr.shape == (3, n_h, dr)
+
+
+def pin_absorb_uq_uk(O):
+    """Brute-force entries of W_UQ_h W_UK_h^T, and c_q (W_UQ_h W_UK_h^T) == (c_q W_UQ_h) W_UK_h^T,
+    the absorbed query's latent part (associativity, to 1e-10)."""
+    r = np.random.default_rng(19)
+    n_h, dh, dc, dcq = 3, 4, 5, 6
+    wuq, wuk = r.standard_normal((dcq, n_h * dh)), r.standard_normal((dc, n_h * dh))
+    w = O.absorb_uq_uk(wuq, wuk, n_h)
+    assert w.shape == (dcq, n_h * dc)
+    for h in range(n_h):
+        for k in range(dcq):
+            for c in range(dc):
+                ref = sum(wuq[k, h * dh + j] * wuk[c, h * dh + j] for j in range(dh))
+                assert abs(w[k, h * dc + c] - ref) < 1e-12
+    cq = r.standard_normal((2, dcq))
+    qn = (cq @ wuq).reshape(2, n_h, dh)
+    qcat = O.absorb_query(qn, np.zeros((2, n_h, 2)), np.zeros(2), wuk, 10000.0)
+    assert np.max(np.abs((cq @ w).reshape(2, n_h, dc) - qcat[..., :dc])) < 1e-10
+
+
 # ------------------------------------------------------------------------------ attention
 
 def pin_attention_bruteforce(O):

@@ -179,6 +179,23 @@ def _decode_blocks_of_16(codes, scale_bytes, fmt):
     return np.ldexp(vals, e[..., :codes.shape[-1]])
 
 
+def _uq_uk_transposed(w_uq, w_uk, n_h):
+    w_uq = np.asarray(w_uq, dtype=np.float64)
+    w_uk = np.asarray(w_uk, dtype=np.float64)
+    d_h = w_uq.shape[1] // n_h
+    return np.concatenate([w_uq[:, h * d_h:(h + 1) * d_h] @ w_uk[:, ((n_h - 1 - h) * d_h):((n_h - h) * d_h)].T
+                           for h in range(n_h)], axis=1)
+
+
+def _compressed_rope_from_x(x, w_dq, w_uq, w_qr, pos, n_h, base):
+    # rope query taken from the first d_cq columns of x instead of from c_q
+    c_q = OR.query_latent(x, w_dq)
+    q, _ = OR.query_projection(c_q, w_uq, w_qr, pos, n_h, base)
+    xs = np.asarray(x, dtype=np.float64)[:, :np.asarray(w_qr).shape[0]]
+    _, qr = OR.query_projection(xs, w_uq, w_qr, pos, n_h, base)
+    return q, qr
+
+
 MUTANTS = {
     "rope_sign_flip": dict(rope_rotate=_rope_sign_flip),
     "rope_half_split": dict(rope_rotate=_rope_half_split),
@@ -200,6 +217,8 @@ MUTANTS = {
     "e4m3_bias_8": dict(fp_element_value=_e4m3_bias8),
     "e2m1_nibbles_swapped": dict(mx_pack_e2m1=_pack_swapped),
     "mx_decode_blocks_of_16": dict(mx_decode_rows=_decode_blocks_of_16),
+    "uq_uk_wrong_head": dict(absorb_uq_uk=_uq_uk_transposed),
+    "compressed_rope_from_x": dict(query_projection_compressed=_compressed_rope_from_x),
 }
 
 
