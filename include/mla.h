@@ -257,6 +257,44 @@ MLA_API mla_status mla_out(const mla_config* cfg, const void* o_lat, const void*
 MLA_API mla_status mla_query_proj(const mla_config* cfg, const void* x, const void* w_q, const void* w_qr,
                           void* q_nope, void* q_rope, int32_t n_tokens, mla_stream_t stream);
 
+/* The query side with compression ([OPN] s.4: "first c_q = x @ W_DQ, then Q = c_q @ W_UQ"; the
+ * query is recomputed from x and never cached).  d_cq is the width of the query latent c_q
+ * (the page gives it as d_c).  The decoupled RoPE query of [GLO] comes from the same latent:
+ * q_rope = c_q @ W_QR.  Two ways to the absorbed query q_cat:
+ *   mla_query_latent -> mla_query_up (q_nope, q_rope) -> mla_absorb_q, or, with W_UQ folded into
+ *   W_UK once (mla_fold_uq_uk, [GLO]/[RMJ] absorption by associativity),
+ *   mla_query_latent -> mla_query_up (q_rope only) -> mla_absorb_q_compressed.
+ * Row widths (d_cq, n_h*d_h, n_h*d_r) must be multiples of 16 bytes (else MLA_ERR_UNSUPPORTED);
+ * n_tokens == 0 is a no-op. */
+/* c_q[n] = x[n] @ W_DQ.  x device [n_tokens, d_model]; w_dq device [d_model, d_cq];
+ * c_q device [n_tokens, d_cq]. */
+MLA_API mla_status mla_query_latent(const mla_config* cfg, int32_t d_cq, const void* x, const void* w_dq,
+                                    void* c_q, int32_t n_tokens, mla_stream_t stream);
+/* q_nope[n] = c_q[n] @ W_UQ and q_rope[n] = c_q[n] @ W_QR (not rotated: mla_absorb_q and
+ * mla_absorb_q_compressed rotate at the token's position).  c_q device [n_tokens, d_cq];
+ * w_uq device [d_cq, n_h*d_h]; w_qr device [d_cq, n_h*d_r]; q_nope device [n_tokens, n_h, d_h];
+ * q_rope device [n_tokens, n_h, d_r].  Either output (with its weight) may be NULL, not both. */
+MLA_API mla_status mla_query_up(const mla_config* cfg, int32_t d_cq, const void* c_q, const void* w_uq,
+                                const void* w_qr, void* q_nope, void* q_rope, int32_t n_tokens,
+                                mla_stream_t stream);
+/* W_UQ folded into W_UK, once when the weights are loaded (not a per-token step):
+ *   w_uqk[:, h*d_c:(h+1)*d_c] = W_UQ[:, h*d_h:(h+1)*d_h] @ W_UK[:, h*d_h:(h+1)*d_h]^T
+ * w_uq device [d_cq, n_h*d_h]; w_uk device [d_c, n_h*d_h]; w_uqk device [d_cq, n_h*d_c] (output;
+ * fp32 accumulation, rounded to cfg->dtype).  For d_cq = d_c the folded weight holds n_h d_c^2
+ * numbers against 2 n_h d_c d_h for the pair: twice the bytes a decode step streams at d_h =
+ * d_c / 4, in exchange for one GEMM per step instead of two. */
+MLA_API mla_status mla_fold_uq_uk(const mla_config* cfg, int32_t d_cq, const void* w_uq, const void* w_uk,
+                                  void* w_uqk, mla_stream_t stream);
+/* The absorbed query from the query latent:
+ *   q_cat[n,h,0:d_c] = c_q[n] @ w_uqk[:, h*d_c:(h+1)*d_c]
+ *   q_cat[n,h,d_c:W] = RoPE(q_rope[n,h,:], pos[n])
+ * c_q device [n_tokens, d_cq]; q_rope device [n_tokens, n_h, d_r] (not rotated); pos device int32
+ * [n_tokens]; w_uqk device [d_cq, n_h*d_c] (from mla_fold_uq_uk); q_cat device [n_tokens, n_h, W].
+ * Same output as mla_absorb_q on q_nope = c_q @ W_UQ, up to rounding. */
+MLA_API mla_status mla_absorb_q_compressed(const mla_config* cfg, int32_t d_cq, const void* c_q,
+                                           const void* q_rope, const int32_t* pos, const void* w_uqk,
+                                           void* q_cat, int32_t n_tokens, mla_stream_t stream);
+
 /* mla_out_proj - the final projection over the concatenated heads ([OPN] s.2 "out = O @ W_O";
  * row block h of W_O belongs to head h):  out[n, :] = o[n, :] @ W_O
  * o device [n_tokens, n_h*d_h] (what mla_out writes); w_o device [n_h*d_h, d_model];

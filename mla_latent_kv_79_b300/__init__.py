@@ -17,7 +17,7 @@ from ._lib import MLAError, MLA_F32, MLA_BF16, MLA_KV_PLAIN, MLA_KV_MXFP8, MLA_K
 
 __all__ = ["MLAConfig", "PagedCache", "mla_cache_append", "mla_absorb_q", "mla_workspace_size",
            "mla_decode", "mla_decode_static", "mla_prefill", "mla_prefill_unabsorbed", "mla_out", "mla_out_proj",
-           "mla_query_proj",
+           "mla_query_proj", "mla_query_latent", "mla_query_up", "mla_fold_uq_uk", "mla_absorb_q_compressed",
            "mla_get_device_error",
            "mla_set_tuning",
            "mla_last_attention_path", "MLAError", "lib"]
@@ -199,6 +199,50 @@ def mla_query_proj(cfg: MLAConfig, x, w_q, w_qr, q_nope=None, q_rope=None, strea
                               _stream(stream))
     _lib.check(st, "mla_query_proj")
     return q_nope, q_rope
+
+
+def mla_query_latent(cfg: MLAConfig, x, w_dq, c_q=None, stream=None):
+    """c_q = x . W_DQ; d_cq is W_DQ's column count."""
+    n, d_cq = x.shape[0], w_dq.shape[1]
+    if c_q is None:
+        c_q = torch.empty((n, d_cq), dtype=cfg.torch_dtype, device=x.device)
+    _lib.check(lib().mla_query_latent(ctypes.byref(cfg.c()), d_cq, _ptr(x), _ptr(w_dq), _ptr(c_q), n, _stream(stream)),
+               "mla_query_latent")
+    return c_q
+
+
+def mla_query_up(cfg: MLAConfig, c_q, w_uq=None, w_qr=None, q_nope=None, q_rope=None, stream=None):
+    """q_nope = c_q . W_UQ (when w_uq is given) and q_rope = c_q . W_QR (when w_qr is given)."""
+    n, d_cq = c_q.shape
+    if w_uq is not None and q_nope is None:
+        q_nope = torch.empty((n, cfg.n_heads, cfg.d_nope), dtype=cfg.torch_dtype, device=c_q.device)
+    if w_qr is not None and q_rope is None:
+        q_rope = torch.empty((n, cfg.n_heads, cfg.d_rope), dtype=cfg.torch_dtype, device=c_q.device)
+    st = lib().mla_query_up(ctypes.byref(cfg.c()), d_cq, _ptr(c_q), _ptr(w_uq), _ptr(w_qr),
+                            _ptr(q_nope) if w_uq is not None else 0, _ptr(q_rope) if w_qr is not None else 0, n,
+                            _stream(stream))
+    _lib.check(st, "mla_query_up")
+    return q_nope, q_rope
+
+
+def mla_fold_uq_uk(cfg: MLAConfig, w_uq, w_uk, w_uqk=None, stream=None):
+    """W_UQ folded into W_UK: [d_cq, n_h * d_c], head h in column block h."""
+    d_cq = w_uq.shape[0]
+    if w_uqk is None:
+        w_uqk = torch.empty((d_cq, cfg.n_heads * cfg.d_latent), dtype=cfg.torch_dtype, device=w_uq.device)
+    _lib.check(lib().mla_fold_uq_uk(ctypes.byref(cfg.c()), d_cq, _ptr(w_uq), _ptr(w_uk), _ptr(w_uqk), _stream(stream)),
+               "mla_fold_uq_uk")
+    return w_uqk
+
+
+def mla_absorb_q_compressed(cfg: MLAConfig, c_q, q_rope, pos, w_uqk, q_cat=None, stream=None):
+    n, d_cq = c_q.shape
+    if q_cat is None:
+        q_cat = torch.empty((n, cfg.n_heads, cfg.width), dtype=cfg.torch_dtype, device=c_q.device)
+    st = lib().mla_absorb_q_compressed(ctypes.byref(cfg.c()), d_cq, _ptr(c_q), _ptr(q_rope), _ptr(pos), _ptr(w_uqk),
+                                       _ptr(q_cat), n, _stream(stream))
+    _lib.check(st, "mla_absorb_q_compressed")
+    return q_cat
 
 
 def mla_out_proj(cfg: MLAConfig, o, w_o, out=None, stream=None):

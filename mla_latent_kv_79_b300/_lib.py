@@ -51,6 +51,10 @@ SIGNATURES = {
     "mla_prefill": (_I, [_CFG, _CACHE, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mla_prefill_unabsorbed_workspace_size": (_I, [_CFG, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "mla_prefill_unabsorbed": (_I, [_CFG, _CACHE, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_query_latent": (_I, [_CFG, _I, _P, _P, _P, _I, _P]),
+    "mla_query_up": (_I, [_CFG, _I, _P, _P, _P, _P, _P, _I, _P]),
+    "mla_fold_uq_uk": (_I, [_CFG, _I, _P, _P, _P, _P]),
+    "mla_absorb_q_compressed": (_I, [_CFG, _I, _P, _P, _P, _P, _P, _I, _P]),
     "mla_out": (_I, [_CFG, _P, _P, _P, _I, _P]),
     "mla_out_proj": (_I, [_CFG, _P, _P, _P, _I, _P]),
     "mla_query_proj": (_I, [_CFG, _P, _P, _P, _P, _P, _I, _P]),

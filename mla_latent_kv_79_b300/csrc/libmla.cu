@@ -52,7 +52,8 @@ static mla_status device_info(DeviceInfo** out) {
                 (const void*)tca::tc_attention_kernel<KV_PLAIN>, (const void*)tca::tc_attention_kernel<KV_MXFP8>,
                 (const void*)tca::tc_attention_kernel<KV_MXFP4>, (const void*)tcg::tc_gemm_kernel<tcg::ABSORB>,
                 (const void*)tcg::tc_gemm_kernel<tcg::OUT>, (const void*)tcg::tc_gemm_kernel<tcg::APPEND>,
-                (const void*)tcg::tc_gemm_kernel<tcg::OPROJ>, (const void*)tcf::prep_kernel,
+                (const void*)tcg::tc_gemm_kernel<tcg::OPROJ>, (const void*)tcg::tc_gemm_kernel<tcg::ABSORBC>,
+                (const void*)tcf::prep_kernel,
                 (const void*)tcf::flash_kernel};
             for (const void* f : fns)
                 if (cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -668,6 +669,109 @@ mla_status mla_query_proj(const mla_config* cfg, const void* x, const void* w_q,
     if ((st = device_info(&dev)) != MLA_OK) return st;
     if ((st = dense_projection(cfg, dev, x, w_q, q_nope, dm, hd, n_tokens, s)) != MLA_OK) return st;
     return dense_projection(cfg, dev, x, w_qr, q_rope, dm, hr, n_tokens, s);
+}
+
+mla_status mla_query_latent(const mla_config* cfg, int32_t d_cq, const void* x, const void* w_dq, void* c_q,
+                            int32_t n_tokens, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0 || d_cq <= 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!x || !w_dq || !c_q || !aligned16(x) || !aligned16(w_dq) || !aligned16(c_q)) return MLA_ERR_INVALID_ARG;
+    const size_t es = elem_size(cfg);
+    if (((size_t)d_cq * es) % 16 || ((size_t)cfg->d_model * es) % 16) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    return dense_projection(cfg, dev, x, w_dq, c_q, cfg->d_model, d_cq, n_tokens, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_query_up(const mla_config* cfg, int32_t d_cq, const void* c_q, const void* w_uq, const void* w_qr,
+                        void* q_nope, void* q_rope, int32_t n_tokens, mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0 || d_cq <= 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!c_q || !aligned16(c_q) || (!q_nope && !q_rope)) return MLA_ERR_INVALID_ARG;
+    if (q_nope && (!w_uq || !aligned16(w_uq) || !aligned16(q_nope))) return MLA_ERR_INVALID_ARG;
+    if (q_rope && (!w_qr || !aligned16(w_qr) || !aligned16(q_rope))) return MLA_ERR_INVALID_ARG;
+    const long long hd = (long long)cfg->n_heads * cfg->d_nope, hr = (long long)cfg->n_heads * cfg->d_rope;
+    const size_t es = elem_size(cfg);
+    if (((size_t)d_cq * es) % 16 || ((size_t)hd * es) % 16 || ((size_t)hr * es) % 16) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    if (q_nope && (st = dense_projection(cfg, dev, c_q, w_uq, q_nope, d_cq, hd, n_tokens, s)) != MLA_OK) return st;
+    if (q_rope && (st = dense_projection(cfg, dev, c_q, w_qr, q_rope, d_cq, hr, n_tokens, s)) != MLA_OK) return st;
+    return MLA_OK;
+}
+
+mla_status mla_fold_uq_uk(const mla_config* cfg, int32_t d_cq, const void* w_uq, const void* w_uk, void* w_uqk,
+                          mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (d_cq <= 0 || !w_uq || !w_uk || !w_uqk) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(w_uq) || !aligned16(w_uk) || !aligned16(w_uqk)) return MLA_ERR_INVALID_ARG;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int n_h = cfg->n_heads, d_h = cfg->d_nope, d_c = cfg->d_latent;
+    // per head h: W_UQK[k, h*d_c + c] = sum_j W_UQ[k, h*d_h + j] * W_UK[c, h*d_h + j]  (a weight-load
+    // step, once; fp32 accumulation)
+    SimtGemmArgs g{};
+    g.A = w_uq; g.lda = (long long)n_h * d_h; g.a_batch = d_h;
+    g.B = w_uk; g.ldb_k = 1; g.ldb_n = (long long)n_h * d_h; g.b_batch = d_h;  // B(j, c) = W_UK[c, h*d_h + j]
+    g.C = w_uqk; g.ldc = (long long)n_h * d_c; g.c_batch = d_c;
+    g.M = d_cq; g.N = d_c; g.K = d_h;
+    dim3 grid((d_c + 63) / 64, (d_cq + 63) / 64, n_h);
+    if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    count_launches(1);
+    return launch_status();
+}
+
+mla_status mla_absorb_q_compressed(const mla_config* cfg, int32_t d_cq, const void* c_q, const void* q_rope,
+                                   const int32_t* pos, const void* w_uqk, void* q_cat, int32_t n_tokens,
+                                   mla_stream_t stream) {
+    mla_status st = check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (n_tokens < 0 || d_cq <= 0) return MLA_ERR_INVALID_ARG;
+    if (n_tokens == 0) return MLA_OK;
+    if (!c_q || !q_rope || !pos || !w_uqk || !q_cat) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(c_q) || !aligned16(q_rope) || !aligned16(w_uqk) || !aligned16(q_cat)) return MLA_ERR_INVALID_ARG;
+    const size_t es = elem_size(cfg);
+    if (((size_t)d_cq * es) % 16) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int n_h = cfg->n_heads, d_c = cfg->d_latent, d_r = cfg->d_rope;
+    const int W = d_c + d_r;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+    const unsigned long long wait_ns = (unsigned long long)g_tune[MLA_TUNE_WAIT_LIMIT_US].load() * 1000ull;
+    if (!g_tune[MLA_TUNE_FORCE_SIMT].load() &&
+        tc_gemm_absorbc_supported(cfg, d_cq, n_tokens, dev->cc_major, dev->cc_minor)) {
+        st = tc_gemm_absorb_compressed(cfg, d_cq, c_q, q_rope, pos, w_uqk, q_cat, n_tokens, gemm_tuning(wait_ns), s);
+        if (st != MLA_OK) return st;
+        count_launches(1);
+        return MLA_OK;
+    }
+    const dim3 blocks(n_tokens, (n_h + ROPE_HEADS - 1) / ROPE_HEADS);
+    RopeFreq rf;
+    rope_freq_fill(&rf, d_r, cfg->rope_base);
+    if (cfg->dtype == MLA_BF16)
+        rope_query_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)q_rope, pos, (bf16*)q_cat, n_tokens, n_h, d_r, d_c, rf);
+    else
+        rope_query_kernel<float><<<blocks, 256, 0, s>>>((const float*)q_rope, pos, (float*)q_cat, n_tokens, n_h, d_r, d_c, rf);
+    count_launches(1);
+    if ((st = launch_status()) != MLA_OK) return st;
+    SimtGemmArgs g{};
+    g.A = c_q; g.lda = d_cq; g.a_batch = 0;                                              // every head reads c_q
+    g.B = w_uqk; g.ldb_k = (long long)n_h * d_c; g.ldb_n = 1; g.b_batch = d_c;          // B(k, c) = W_UQK[k, h*d_c + c]
+    g.C = q_cat; g.ldc = (long long)n_h * W; g.c_batch = W;
+    g.M = n_tokens; g.N = d_c; g.K = d_cq;
+    dim3 grid((d_c + 63) / 64, (n_tokens + 63) / 64, n_h);
+    if (cfg->dtype == MLA_BF16) simt_gemm_kernel<bf16, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    else simt_gemm_kernel<float, EPI_STORE><<<grid, 256, 0, s>>>(g);
+    count_launches(1);
+    return launch_status();
 }
 
 mla_status mla_get_device_error(mla_stream_t stream) {

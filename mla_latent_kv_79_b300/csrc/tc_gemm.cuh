@@ -5,6 +5,8 @@
 //   append: row[n, c] = sum_k [W_DKV | W_KR][k, c] * x[n, k], stored to the paged pool with
 //           RoPE(., pos[n]) on the last d_r columns                            (M = c, K = k)
 //   oproj:  out[n, m] = sum_k W_O[k, m] * o[n, k], k over n_h*d_h               (M = m, K = k)
+//   absorbc: q_cat[n, h, c] = sum_k W_UQK[k, h*d_c + c] * c_q[n, k], the absorbed query from the
+//           compressed query latent with W_UQ folded into W_UK (RoPE half as in absorb) (M = c, K = k)
 //
 // All are computed "weights as M, tokens as N": D[m, n] = sum_k A[m, k] * B[n, k] with a
 // 128-row weight tile as A (K-major for W_UK, MN-major for W_UV, W_DKV, W_KR and W_O, as the
@@ -64,7 +66,7 @@ inline int max_heads_per_cta(int n_pad) {
     return h < HPC ? h : HPC;
 }
 
-enum Mode { ABSORB = 0, OUT = 1, APPEND = 2, OPROJ = 3 };
+enum Mode { ABSORB = 0, OUT = 1, APPEND = 2, OPROJ = 3, ABSORBC = 4 };
 
 struct GemmArgs {
     int mode;
@@ -134,11 +136,11 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, unsigned lo
 // index within the CTA's K range.
 template <int MODE>
 __device__ __forceinline__ int chunk_head(int c, int nh, int kper) {
-    return MODE == OUT ? c % nh : c / kper;
+    return (MODE == OUT || MODE == ABSORBC) ? c % nh : c / kper;
 }
 template <int MODE>
 __device__ __forceinline__ int chunk_k(int c, int nh, int kper) {
-    return MODE == OUT ? c / nh : c % kper;
+    return (MODE == OUT || MODE == ABSORBC) ? c / nh : c % kper;
 }
 
 // Pool row (element offset) of appended token n, or -1 (and the bounds error) when its sequence,
@@ -238,7 +240,7 @@ __device__ __forceinline__ void split_store(const GemmArgs& g, uint32_t base, co
                 if (r0 + r < KS) v += part[r];
         }
         const int n = n0 + nl;
-        if (MODE == ABSORB) {
+        if (MODE == ABSORB || MODE == ABSORBC) {
             out[((size_t)n * g.n_h + h0) * g.width + mt * BM + tid] = __float2bfloat16_rn(v);
         } else if (MODE == OUT || MODE == OPROJ) {  // OPROJ: n_h = 1, d_h = d_model
             out[(size_t)n * g.n_h * g.d_h + (size_t)h0 * g.d_h + mt * BM + tid] = __float2bfloat16_rn(v);
@@ -342,14 +344,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ptx::tma_load_2d(st, t, m0, kc * BK, fb);
                 ptx::tma_load_2d(st + BK * 128, t, m0 + 64, kc * BK, fb);
             } else {
-                // W_UV rows c in [kc*64, +64) x cols h*d_h + mt*128 + {0, 64} (MN-major, two boxes)
+                // W_UV rows c in [kc*64, +64) x cols h*d_h + mt*128 + {0, 64} (MN-major, two boxes);
+                // ABSORBC: W_UQK rows k x cols h*d_c + ... (d_h holds d_c in that mode)
                 ptx::tma_load_2d(st, &tmA, h * g.d_h + mt * BM, kc * BK, fb);
                 ptx::tma_load_2d(st + BK * 128, &tmA, h * g.d_h + mt * BM + 64, kc * BK, fb);
             }
         };
         auto load_b = [&](int c, uint32_t st, uint32_t fb) {
             const int h = h0 + chunk_head<MODE>(c, nh, kper), kc = kc0 + chunk_k<MODE>(c, nh, kper);
-            // q_nope viewed [n, n_h*d_h] (ABSORB), o_lat viewed [n, n_h*d_c] (OUT) or x [n, d_model]
+            // q_nope viewed [n, n_h*d_h] (ABSORB), o_lat viewed [n, n_h*d_c] (OUT); x [n, d_model]
+            // (APPEND, OPROJ) and c_q [n, d_cq] (ABSORBC) are shared by every head
             const int col = (MODE == ABSORB ? h * g.d_h : MODE == OUT ? h * g.d_c : 0) + kc * BK;
             ptx::tma_load_2d(st + A_BYTES, &tmB, col, n0, fb);
         };
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;  // m within the tile
-        if (MODE == ABSORB && g.q_rope) {
+        if ((MODE == ABSORB || MODE == ABSORBC) && g.q_rope) {
             grid_dependency_wait();  // q_rope and pos come from earlier kernels
             absorb_rope(g, n0, threadIdx.x - 64);
         }
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int n = n0 + c0 + i;
                         if (c0 + i < g.n_pad && n < g.n_tokens) {
                             const bf16 v = __float2bfloat16_rn(__uint_as_float(r[i]));
-                            if (MODE == ABSORB)
+                            if (MODE == ABSORB || MODE == ABSORBC)
                                 out[((size_t)n * g.n_h + h) * g.width + mt * BM + row] = v;
                             else
                                 out[(size_t)n * g.n_h * g.d_h + (size_t)h * g.d_h + mt * BM + row] = v;
@@ -608,6 +612,7 @@ inline mla_status launch(const GemmArgs& g0, const CUtensorMap& a, const CUtenso
         g.mode == ABSORB ? tc_gemm_kernel<ABSORB>
         : g.mode == OUT  ? tc_gemm_kernel<OUT>
         : g.mode == OPROJ ? tc_gemm_kernel<OPROJ>
+        : g.mode == ABSORBC ? tc_gemm_kernel<ABSORBC>
                           : tc_gemm_kernel<APPEND>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return MLA_ERR_CUDA;
@@ -687,6 +692,36 @@ inline mla_status tc_gemm_out(const mla_config* c, const void* o_lat, const void
         !tcg::encode_2d(&tb, o_lat, hc, (uint64_t)n, hc, (uint32_t)g.n_pad))
         return MLA_ERR_CUDA;
     return tcg::launch(g, ta, tb, ta, c->d_nope / tcg::BM, c->n_heads, t, stream);
+}
+
+inline bool tc_gemm_absorbc_supported(const mla_config* c, int d_cq, int n, int cc_major, int cc_minor) {
+    return c->dtype == MLA_BF16 && cc_major == 10 && cc_minor == 3 && n > 0 && d_cq % 64 == 0 &&
+           c->d_latent % 128 == 0 && c->d_rope % 2 == 0 && (c->d_rope * 2) % 16 == 0;
+}
+
+// The absorbed query from the compressed query latent: one CTA per (128 latent columns, head,
+// token tile), W_UQK's head slab as the MN-major A operand (the OUT mode's addressing with
+// d_h := d_c), c_q as B for every head, the ABSORB mode's epilogue and RoPE half.
+inline mla_status tc_gemm_absorb_compressed(const mla_config* c, int d_cq, const void* c_q, const void* q_rope,
+                                            const int* pos, const void* w_uqk, void* q_cat, int n,
+                                            const tcg::Tuning& t, cudaStream_t stream) {
+    tcg::GemmArgs g{};
+    g.mode = tcg::ABSORBC;
+    g.n_tokens = n;
+    g.q_rope = reinterpret_cast<const bf16*>(q_rope);
+    g.pos = pos;
+    g.d_r = c->d_rope;
+    rope_freq_fill(&g.rf, c->d_rope, c->rope_base);
+    g.n_pad = tcg::n_pad_for(n);
+    g.k_chunks = d_cq / tcg::BK;
+    g.n_h = c->n_heads; g.d_h = c->d_latent; g.d_c = c->d_latent; g.width = c->d_latent + c->d_rope;
+    g.out = q_cat;
+    const uint64_t hc = (uint64_t)c->n_heads * c->d_latent;
+    CUtensorMap ta, tb;
+    if (!tcg::encode_2d(&ta, w_uqk, hc, (uint64_t)d_cq, hc, 64) ||
+        !tcg::encode_2d(&tb, c_q, (uint64_t)d_cq, (uint64_t)n, (uint64_t)d_cq, (uint32_t)g.n_pad))
+        return MLA_ERR_CUDA;
+    return tcg::launch(g, ta, tb, ta, c->d_latent / tcg::BM, c->n_heads, t, stream);
 }
 
 // a dense projection out[n, :] = in[n, :] . W with W [K, M] row-major (M contiguous), the
