@@ -323,6 +323,14 @@ def config_of(name, case, out_proj=False):
             "l2": "flushed between steps (256 MB write, then read back so no dirty lines remain)"}
 
 
+def query_config(query: str) -> dict:
+    if query == "given":
+        return {}
+    return {"query": {"direct": "x . W_Q, x . W_QR, then absorb_q (in the step)",
+                      "compressed": "c_q = x . W_DQ, RoPE query c_q . W_QR, absorbed query from c_q with "
+                                    "W_UQ folded into W_UK (in the step; d_cq = d_c)"}[query]}
+
+
 # ------------------------------------------------------------------------------------ our arm
 
 def run_ours(args):
@@ -382,6 +390,25 @@ def run_ours(args):
         nb = ctypes.c_size_t(0)
         M.lib().mla_prefill_unabsorbed_workspace_size(ctypes.byref(cfg.c()), 0, B, ctypes.byref(nb))
         uws = torch.empty(int(nb.value), dtype=torch.uint8, device="cuda")
+    # the query side of the step: given (q_nope, q_rope as inputs), direct (x . W_Q, x . W_QR) or
+    # compressed (c_q = x . W_DQ, RoPE query c_q . W_QR, absorbed query with W_UQ folded into W_UK)
+    if args.query != "given":
+        qrng = np.random.default_rng(7 + B)
+        xq = dev(W.quantise(W.normal(qrng, (B, s.d_model)), dt))
+        if args.query == "direct":
+            w_q = dev(W.weight(qrng, s.d_model, s.n_heads * s.d_nope, dt))
+            w_qr = dev(W.weight(qrng, s.d_model, s.n_heads * s.d_rope, dt))
+        else:
+            d_cq = s.d_latent
+            w_dq = dev(W.weight(qrng, s.d_model, d_cq, dt))
+            w_qr = dev(W.weight(qrng, d_cq, s.n_heads * s.d_rope, dt))
+            w_uqk = M.mla_fold_uq_uk(cfg, dev(W.weight(qrng, d_cq, s.n_heads * s.d_nope, dt)), w_uk)
+            c_q = torch.empty((B, d_cq), dtype=cfg.torch_dtype, device="cuda")
+        qn_buf = torch.empty_like(q_nope)
+        qr_buf = torch.empty_like(q_rope)
+        q_in = (xq,)
+    else:
+        q_in = (q_nope, q_rope)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     flush_words = flush.view(torch.int64)
     stream = torch.cuda.current_stream()
@@ -393,15 +420,24 @@ def run_ours(args):
         flush.zero_()
         flush_words.sum()
 
-    def step(qn=q_nope, qr=q_rope, xx=None, oo=o, ll=lse, ff=out):
+    def step(qi=q_in, xx=None, oo=o, ll=lse, ff=out):
         if appending:  # the same positions every step: the cache ends each step identical
             M.mla_cache_append(cfg, cache, x if xx is None else xx, w_dkv, w_kr, a_seq, a_pos, stream=stream)
+        if args.query == "direct":
+            qn, qr = M.mla_query_proj(cfg, qi[0], w_q, w_qr, q_nope=qn_buf, q_rope=qr_buf, stream=stream)
+        elif args.query == "compressed":
+            M.mla_query_latent(cfg, qi[0], w_dq, c_q=c_q, stream=stream)
+            M.mla_query_up(cfg, c_q, None, w_qr, q_rope=qr_buf, stream=stream)
+            M.mla_absorb_q_compressed(cfg, c_q, qr_buf, pos, w_uqk, q_cat=q_cat, stream=stream)
+        else:
+            qn, qr = qi
         if unabsorbed:
             M.mla_prefill_unabsorbed(cfg, cache, 0, 0, qn, qr, w_uk, w_uv, o=oo, lse=ll, workspace=uws, stream=stream)
             if args.out_proj:
                 M.mla_out_proj(cfg, oo, w_o, out=ff, stream=stream)
             return
-        M.mla_absorb_q(cfg, qn, qr, pos, w_uk, q_cat=q_cat, stream=stream)
+        if args.query != "compressed":
+            M.mla_absorb_q(cfg, qn, qr, pos, w_uk, q_cat=q_cat, stream=stream)
         if prefill:
             M.mla_prefill(cfg, cache, 0, 0, q_cat, o_lat=o_lat, lse=ll, workspace=ws, stream=stream)
         else:
@@ -468,7 +504,7 @@ def run_ours(args):
             buf = buf.pin_memory()
         views = [buf[o_:o_ + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o_, t in zip(offs, tensors)]
         return buf, views
-    ins = [q_nope, q_rope] + ([x] if appending else [])
+    ins = list(q_in) + ([x] if appending else [])
     d_in, e_in = staging(ins, pinned=False)
     h_in, h_in_views = staging(ins, pinned=True)
     for hv, t in zip(h_in_views, ins):
@@ -488,7 +524,8 @@ def run_ours(args):
         flush_l2()
         eev[i][0].record(stream)
         d_in.copy_(h_in, non_blocking=True)
-        step(e_in[0], e_in[1], e_in[2] if appending else None, e_o, e_lse, e_f)
+        nq = len(q_in)
+        step(tuple(e_in[:nq]), e_in[nq] if appending else None, e_o, e_lse, e_f)
         h_out.copy_(d_out, non_blocking=True)
         eev[i][1].record(stream)
     torch.cuda.synchronize()
@@ -520,7 +557,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": config_of(args.workload, case, args.out_proj),
+        "config": {**config_of(args.workload, case, args.out_proj), **query_config(args.query)},
         "roofline": {"bound": "tensor" if tensor_bound else "hbm",
                      "achieved": alg_flops / k_mean_s / 1e12 if tensor_bound else achieved,
                      "peak": tflops if tensor_bound else hbm, "unit": "TFLOP/s" if tensor_bound else "GB/s",
@@ -554,6 +591,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_b16_l4096", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--query", default="given", choices=["given", "direct", "compressed"],
+                    help="query side in the step: given q_nope/q_rope, or from x (direct or compressed)")
     ap.add_argument("--out-proj", action="store_true",
                     help="add the output projection over the heads (W_O) to the timed step")
     args = ap.parse_args()
