@@ -10,19 +10,22 @@
 // pairs) and the 128 x 512 fp32 output accumulator:
 //
 //   score CTA (rank 0)  TMEM: Q [0,288), S double buffer [288,416)
-//     S = Q . page^T over all 576 columns, online softmax (running max raised only when it
-//     grows by more than 2^8: O and l share the stale max, so the result is exact), then
-//     P (bf16, 16 KB) plus (alpha, l) per head are stored with st.async straight into the
-//     value CTA's shared memory, completing bytes on its mbarrier.
+//     S = Q . page^T over all 576 columns, issued by two warps taking alternate pages (warp 1
+//     the even pages into score buffer 0, warp 6 the odd ones into buffer 1), online softmax
+//     (running max raised only when it grows by more than 2^8: O and l share the stale max, so
+//     the result is exact), then P (bf16, 16 KB) plus (alpha, l) per head are stored with
+//     st.async straight into one of the value CTA's four P buffers, completing bytes on its
+//     mbarrier.
 //   value CTA (rank 1)  TMEM: O [0,512)
 //     rescales O rows when alpha != 1, then O += P . page[:, 0:512] with P as the
 //     shared-memory A operand; drains O / l at the end of every segment.
 //
-// Each CTA streams the page through its own 3-stage TMA ring (the score CTA all 576 columns,
-// the value CTA the 512 latent ones), so the score CTA recycles a stage right after its QK
-// instead of holding it until the value CTA's PV; the value CTA's copy of the latent columns
-// is read while the line is still in L2.  The score-to-value traffic is one-directional, so
-// neither CTA waits on a round trip.
+// Each CTA streams the page through its own TMA ring: the score CTA all 576 columns in 3
+// stages, so that it recycles a stage right after its QK instead of holding it until the
+// value CTA's PV; the value CTA the 512 latent columns in 2 stages, read while the lines are
+// still in L2, which leaves room for four P buffers.  The score-to-value traffic is
+// one-directional and four P buffers deep, so the st.async transfer and the release of a
+// buffer back to the score CTA (each about a microsecond between SMs) stay off the pace.
 //
 // The query of a segment travels through the score CTA's ring too: two items of nine 64-row x
 // 64-column boxes (144 KB, exactly two stages), so that the query and the segment's first page
@@ -31,8 +34,17 @@
 //
 // Roles (224 threads per CTA): warp 0 TMA, warp 1 TMEM allocation and MMA issue, warps 2-5
 // (one TMEM lane quarter each, one head per thread) softmax in the score CTA, rescale and
-// drain in the value CTA; warp 6 of the value CTA hands P buffers back to the score CTA as
-// their PVs complete.  Every wait is bounded.
+// drain in the value CTA; warp 6 issues the odd pages' score MMAs in the score CTA and hands P
+// buffers back to the score CTA as their PVs complete in the value CTA.  Every wait is bounded.
+//
+// The MMA issuers run as whole warps: every lane computes the (warp-uniform) descriptors and
+// one elected lane issues.  Issuing from a single active lane cost sub-partition issue slots
+// that the softmax warps need (measured on B300: 8 % of the B=16 x 4096 decode and 20 % of the
+// ragged B=256 one).
+//
+// In the score CTA the two issuers skip each other's pages, so a page's full barrier is one of
+// (stage, issuer) and a query item's one of its stage: a parity wait is only unambiguous for a
+// waiter that sees every phase of its barrier in order.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -55,25 +67,28 @@ constexpr int V_STAGE_BYTES = LAT_CHUNKS * CHUNK; // value CTA: latent part (64 
 constexpr int P_BYTES = NH * 128;                 // P [128 heads x 64 tokens] bf16, SW128 K-major
 constexpr int META_BYTES = NH * 8;                // (alpha, l) per head, fp32
 constexpr int PBUF_BYTES = P_BYTES + META_BYTES;
-constexpr int R_BYTES = 2 * PBUF_BYTES;
+constexpr int MAX_PBUF = 4;
 constexpr int HALF = 32;                          // MX caches: cache rows per raw item (half a page)
 constexpr int MAX_RAW = 6;
 enum {
-    B_FULL = 0,                      // [STAGES] page landed in this CTA's ring
+    B_FULL = 0,                      // [STAGES] item landed: a page (value CTA) or a query item (score CTA)
     B_EMPTY = B_FULL + MAX_STAGES,   // [STAGES] this CTA's consumer released the stage
     B_SFULL = B_EMPTY + MAX_STAGES,  // [2] score CTA: S buffer written
     B_SFREE = B_SFULL + 2,           // [2] score CTA: S buffer read by the 4 softmax warps
-    B_PFULL = B_SFREE + 2,           // [2] value CTA: P + meta landed (own expect_tx + bytes)
-    B_PEMPTY = B_PFULL + 2,          // [2] score CTA: value CTA's PV finished with P buffer b
-    B_PREADY = B_PEMPTY + 2,         // [2] value CTA: O rescaled, P buffer b ready for the MMA
-    B_PVDONE = B_PREADY + 2,         // [2] value CTA: PV of the page that used P buffer b complete
-    B_OFREE = B_PVDONE + 2,          // value CTA: O drained
+    B_PFULL = B_SFREE + 2,           // [NPBUF] value CTA: P + meta landed (own expect_tx + bytes)
+    B_PEMPTY = B_PFULL + MAX_PBUF,   // [NPBUF] score CTA: value CTA's PV finished with P buffer b
+    B_PREADY = B_PEMPTY + MAX_PBUF,  // [NPBUF] value CTA: O rescaled, P buffer b ready for the MMA
+    B_PVDONE = B_PREADY + MAX_PBUF,  // [NPBUF] value CTA: PV of the page that used P buffer b complete
+    B_OFREE = B_PVDONE + MAX_PBUF,   // value CTA: O drained
     B_DONE = B_OFREE + 1,            // MMA drain at exit
     B_QREADY = B_DONE + 1,           // score CTA: the segment's query is in TMEM (4 softmax warps)
     B_RFULL = B_QREADY + 1,          // MX caches: [RAW_STAGES] raw half page landed
     B_REMPTY = B_RFULL + MAX_RAW,    // MX caches: [RAW_STAGES] the 4 converter warps read it
-    NBARS = B_REMPTY + MAX_RAW
+    B_FULLP = B_REMPTY + MAX_RAW,    // score CTA: [STAGES][2] page of issuer i landed in a stage
+    B_QSEEN = B_FULLP + 2 * MAX_STAGES,  // score CTA: both issuers saw the segment's query
+    NBARS = B_QSEEN + 1
 };
+static_assert(NBARS <= 64, "the producer tracks full barriers in 64-bit masks");
 
 // Shared-memory layout per cache format (KVF: KV_PLAIN, KV_MXFP8, KV_MXFP4).  Both CTAs of a
 // pair use the same offsets.  The plain cache streams bf16 pages by TMA into a 3-stage ring.
@@ -82,8 +97,11 @@ enum {
 // the TMA writes, so the MMA and softmax code is shared.
 template <int KVF>
 struct Lay {
-    static constexpr int STAGES = KVF == KV_PLAIN ? 3 : 2;
-    static constexpr int OFF_R = STAGES * V_STAGE_BYTES;           // value CTA: P buffers
+    static constexpr int STAGES = KVF == KV_PLAIN ? 3 : 2;         // score CTA ring
+    static constexpr int VSTAGES = 2;                              // value CTA ring
+    static constexpr int NPBUF = KVF == KV_PLAIN ? 4 : 2;          // P buffers in the value CTA
+    static constexpr int R_BYTES = NPBUF * PBUF_BYTES;
+    static constexpr int OFF_R = VSTAGES * V_STAGE_BYTES;          // value CTA: P buffers
     static constexpr int ROW_BYTES = KVF == KV_MXFP4 ? WID / 2 : WID;  // code bytes per cache row
     static constexpr int RAW_CODES = HALF * ROW_BYTES;
     static constexpr int RAW_SCALES = HALF * (WID / MX_BLOCK);
@@ -100,6 +118,8 @@ struct Lay {
     static constexpr int NTHREADS = KVF == KV_PLAIN ? 224 : 352;   // + 4 converter warps
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(RAW_STAGES <= MAX_RAW, "raw ring barriers");
+    static_assert(NPBUF <= MAX_PBUF && VSTAGES <= MAX_STAGES, "ring barriers");
+    static_assert(KVF == KV_PLAIN || VSTAGES == STAGES, "the MX converters run one ring depth in both CTAs");
     static_assert(RAW_CODES % 16 == 0 && RAW_SCALES % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
 constexpr int TM_Q = 0, TM_S = 288, TM_O = 0;
@@ -166,6 +186,13 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
     return base + Lay<KVF>::OFF_BARS + 8u * (uint32_t)i;
 }
 
+// The full barrier of a ring item and the bit that tracks its parity in a waiter's or filler's
+// 32-bit mask: a query item's is its stage's (score CTA) and a page's is (stage, page parity)
+// in the score CTA, its stage's in the value CTA.
+__device__ __forceinline__ int full_index(uint32_t rank, bool query, uint32_t stage, uint32_t page) {
+    return (rank == 0 && !query) ? B_FULLP + 2 * (int)stage + (int)(page & 1u) : B_FULL + (int)stage;
+}
+
 // ----------------------------------------------------------------------------- warp 0: TMA
 // Both CTAs run the same page sequence.  Plain cache: the score CTA loads the segment's query
 // and then all nine 64-column chunks of each page, the value CTA the eight latent chunks, by
@@ -173,13 +200,15 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
 // (32 rows of codes, then their scale bytes, both contiguous in the pool) into the raw ring; the
 // converter warps fill every item of the bf16 ring, the query's too (a parity wait on a ring
 // barrier is only unambiguous for a party that fills every item of the ring in order).
-template <int KVF>
+template <int KVF, int STAGES>  // STAGES: depth of this CTA's bf16 ring
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tm, const CUtensorMap* tmq, UnitCursor c,
                                          uint32_t base, uint32_t rank, const WaitCtl& wc) {
     using L = Lay<KVF>;
-    constexpr int STAGES = L::STAGES;
     uint32_t g = 0;       // plain cache: bf16 ring items (queries and pages), in ring order
+    uint32_t gp = 0;      // pages
     uint32_t r = 0;       // MX cache: raw items issued
+    uint64_t fpar = 0;    // plain cache: parity of the next phase of each full barrier (bit = index)
+    uint64_t armed = 0;   // plain cache: full barriers armed at least once
     bool ok = true;
     Segment sg;
     const int nch = rank == 0 ? 9 : LAT_CHUNKS;
@@ -200,7 +229,10 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             for (int qi = 0; qi < Q_ITEMS; ++qi, ++g) {
                 const uint32_t stage = g % STAGES;
                 if (!wait_bar(bar_addr<KVF>(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
-                const uint32_t fb = bar_addr<KVF>(base, B_FULL + stage), dst = base + stage * S_STAGE_BYTES;
+                const int fi = full_index(rank, true, stage, gp);
+                const uint32_t fb = bar_addr<KVF>(base, fi), dst = base + stage * S_STAGE_BYTES;
+                fpar ^= 1ull << fi;
+                armed |= 1ull << fi;
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)S_STAGE_BYTES);
                 for (int j = 0; j < 9; ++j) {
                     const int b = 9 * qi + j;
@@ -209,7 +241,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             }
             if (!ok) break;
         }
-        for (int pg = pg0; pg < sg.page_end; ++pg, ++g) {
+        for (int pg = pg0; pg < sg.page_end; ++pg, ++g, ++gp) {
             int page = __ldg(a.page_table + (long long)sg.seq * a.max_pages + pg);
             if (page < 0 || page >= a.num_pages) {
                 set_device_error(MLA_ERR_DEVICE_BOUNDS);
@@ -218,7 +250,10 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             if (KVF == KV_PLAIN) {
                 const uint32_t stage = g % STAGES;
                 if (!wait_bar(bar_addr<KVF>(base, B_EMPTY + stage), ((g / STAGES) & 1u) ^ 1u, wc)) { ok = false; break; }
-                const uint32_t fb = bar_addr<KVF>(base, B_FULL + stage);
+                const int fi = full_index(rank, false, stage, gp);
+                const uint32_t fb = bar_addr<KVF>(base, fi);
+                fpar ^= 1ull << fi;
+                armed |= 1ull << fi;
                 ptx::mbar_arrive_expect_tx(fb, stage_bytes);
                 const uint32_t dst = base + stage * stage_bytes;
                 for (int cc = 0; cc < nch; ++cc) ptx::tma_load_2d(dst + cc * CHUNK, tm, cc * 64, page * PAGE, fb);
@@ -246,9 +281,9 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         WaitCtl w2 = wc;
         w2.ignore_abort = true;
         w2.limit_ns = 20000000ull;
-        if (KVF == KV_PLAIN) {
-            for (uint32_t k = g > (uint32_t)STAGES ? g - STAGES : 0u; k < g; ++k)
-                wait_bar(bar_addr<KVF>(base, B_FULL + k % STAGES), (k / STAGES) & 1u, w2);
+        if (KVF == KV_PLAIN) {  // the last phase armed on each full barrier
+            for (int i = 0; i < NBARS; ++i)
+                if ((armed >> i) & 1ull) wait_bar(bar_addr<KVF>(base, i), (uint32_t)((fpar >> i) & 1ull) ^ 1u, w2);
         } else {
             for (uint32_t k = r > (uint32_t)L::RAW_RING ? r - L::RAW_RING : 0u; k < r; ++k)
                 wait_bar(bar_addr<KVF>(base, B_RFULL + k % L::RAW_RING), (k / L::RAW_RING) & 1u, w2);
@@ -280,8 +315,8 @@ __device__ __forceinline__ void converter(const AttnArgs& a, const CUtensorMap* 
     const int n_items = HALF * G;
     const int ctid = cw * 32 + lane;
     const uint32_t stage_bytes = rank == 0 ? S_STAGE_BYTES : V_STAGE_BYTES;
-    uint32_t k = 0, r = 0;  // bf16 ring items, raw items
-    uint32_t q_end = 0;     // warp 7: one past the last query item loaded
+    uint32_t k = 0, r = 0, gp = 0;  // bf16 ring items, raw items, pages
+    uint32_t qpar = 0, qarmed = 0;  // warp 7: next phase parity / armed, per stage, of the query barriers
     bool ok = true, waited = false;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
@@ -305,7 +340,8 @@ __device__ __forceinline__ void converter(const AttnArgs& a, const CUtensorMap* 
                             const int b = 9 * qi + j;
                             ptx::tma_load_2d(dst + j * CHUNK, tmq, (b >> 1) * 64, sg.q * NH + (b & 1) * 64, fb);
                         }
-                        q_end = k + 1;
+                        qpar ^= 1u << stage;
+                        qarmed |= 1u << stage;
                     } else {
                         ptx::mbar_arrive(fb);
                     }
@@ -314,7 +350,7 @@ __device__ __forceinline__ void converter(const AttnArgs& a, const CUtensorMap* 
             }
             if (!ok) break;
         }
-        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++k) {
+        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++k, ++gp) {
             const uint32_t stage = k % STAGES;
             if (!warp_wait(bar_addr<KVF>(base, B_EMPTY + stage), ((k / STAGES) & 1u) ^ 1u, wc, false, lane)) {
                 ok = false;
@@ -370,38 +406,54 @@ __device__ __forceinline__ void converter(const AttnArgs& a, const CUtensorMap* 
             if (!ok) break;
             ptx::fence_proxy_async();  // the tensor core reads the stage through the async proxy
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_FULL + stage));
+            if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, full_index(rank, false, stage, gp)));
         }
     }
     if (!ok && cw == 0 && lane == 0) {  // let query loads still in flight land (bounded)
         WaitCtl w2 = wc;
         w2.ignore_abort = true;
         w2.limit_ns = 20000000ull;
-        for (uint32_t q = q_end > (uint32_t)Q_ITEMS ? q_end - Q_ITEMS : 0u; q < q_end; ++q)
-            wait_bar(bar_addr<KVF>(base, B_FULL + q % STAGES), (q / STAGES) & 1u, w2);
+        for (int st = 0; st < STAGES; ++st)
+            if ((qarmed >> st) & 1u) wait_bar(bar_addr<KVF>(base, B_FULL + st), ((qpar >> st) & 1u) ^ 1u, w2);
     }
 }
 
 // ----------------------------------------------------------------------------- score CTA
-template <int KVF>
+// Two issuing threads (warp 1 and warp 6, lane 0) split the pages: ISSUER takes the pages with
+// page index % 2 == ISSUER, always into score buffer ISSUER.  One thread issuing all 36 MMAs of
+// a page was the pace setter (about 88 cycles per N=64 MMA beside the softmax warps); two
+// threads keep the tensor pipe fed.  Each waits only on its own barriers: a page's full
+// barrier of (stage, issuer), its score buffer's free barrier, and the query barriers, which
+// both see every phase of (QSEEN keeps the next query out of TMEM until both saw this one).
+template <int KVF, int ISSUER>
 __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
-                                          const WaitCtl& wc) {
+                                          const WaitCtl& wc, int lane) {
     constexpr int STAGES = Lay<KVF>::STAGES;
+    constexpr uint32_t sb = ISSUER;
     uint32_t g = 0, k = 0, segn = 0;  // pages, ring items, segments
+    uint32_t pbits = 0;               // parity of the next phase of this issuer's page barrier, per stage
+    uint32_t uses = 0;                // pages issued into this issuer's score buffer
     bool ok = true;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
         // the softmax warps put the segment's query into TMEM columns [TM_Q, TM_Q + 288) (they
         // do so only after reading the previous segment's last scores, i.e. after its QKs);
-        // then the three ring stages that carried it are free
-        if (!wait_bar(bar_addr<KVF>(base, B_QREADY), segn & 1u, wc)) break;
+        // then the stages that carried it are free
+        if (!warp_wait(bar_addr<KVF>(base, B_QREADY), segn & 1u, wc, false, lane)) break;
         ptx::tc_fence_after();
-        for (int qi = 0; qi < Q_ITEMS; ++qi, ++k) ptx::mbar_arrive(bar_addr<KVF>(base, B_EMPTY + k % STAGES));
+        if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_QSEEN));
+        if (ISSUER == 0)
+            for (int qi = 0; qi < Q_ITEMS; ++qi)
+                if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_EMPTY + (k + qi) % STAGES));
+        k += Q_ITEMS;
         ++segn;
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
-            const uint32_t stage = k % STAGES, sb = g & 1u;
-            if (!wait_bar(bar_addr<KVF>(base, B_FULL + stage), (k / STAGES) & 1u, wc)) { ok = false; break; }
-            if (!wait_bar(bar_addr<KVF>(base, B_SFREE + sb), ((g >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
+            if ((g & 1u) != sb) continue;  // the other issuer's page
+            const uint32_t stage = k % STAGES;
+            if (!warp_wait(bar_addr<KVF>(base, B_FULLP + 2 * stage + sb), (pbits >> stage) & 1u, wc, false, lane)) { ok = false; break; }
+            pbits ^= 1u << stage;
+            if (!warp_wait(bar_addr<KVF>(base, B_SFREE + sb), (uses & 1u) ^ 1u, wc, false, lane)) { ok = false; break; }
+            ++uses;
             ptx::tc_fence_after();
             // descriptors are the stage's base descriptor plus compile-time offsets (the 14-bit
             // address field cannot carry: shared addresses are < 256 KB).  The 36 MMAs are fully
@@ -413,20 +465,22 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
             for (int cc = 0; cc < 9; ++cc) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA, 4 per 64-column chunk
-                    ptx::mma_ts(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
+                    ptx::mma_ts_elect(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
                                 IDESC_QK, (cc | kk) ? 1u : 0u);
             }
-            ptx::tc_commit(bar_addr<KVF>(base, B_SFULL + sb));
-            ptx::tc_commit(bar_addr<KVF>(base, B_EMPTY + stage));
+            ptx::tc_commit_elect(bar_addr<KVF>(base, B_SFULL + sb));
+            ptx::tc_commit_elect(bar_addr<KVF>(base, B_EMPTY + stage));
         }
     }
-    // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
-    // whatever the configured limit (which may be microseconds when a caller tests timeouts)
-    ptx::tc_commit(bar_addr<KVF>(base, B_DONE));
+    // every MMA this thread issued completes before the CTA frees its TMEM (the drain barrier
+    // counts both issuers): a fixed 20 ms bound, whatever the configured limit (which may be
+    // microseconds when a caller tests timeouts)
+    __syncwarp();
+    ptx::tc_commit_elect(bar_addr<KVF>(base, B_DONE));
     WaitCtl w2 = wc;
     w2.ignore_abort = true;
     w2.limit_ns = 20000000ull;
-    wait_bar(bar_addr<KVF>(base, B_DONE), 0, w2);
+    warp_wait(bar_addr<KVF>(base, B_DONE), 0, w2, false, lane);
 }
 
 template <int KVF>
@@ -434,6 +488,7 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
                                               uint32_t peer, int warp, int lane, const WaitCtl& wc) {
     constexpr int STAGES = Lay<KVF>::STAGES;
     constexpr int OFF_R = Lay<KVF>::OFF_R;
+    constexpr uint32_t NPBUF = Lay<KVF>::NPBUF;
     const AttnArgs& a = args.a;
     const int qd = warp & 3;  // TMEM lane quarter this warp may access
     const int h = qd * 32 + lane;
@@ -442,7 +497,8 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
     const uint32_t pbuf_r = ptx::mapa(base + OFF_R, peer);          // value CTA's P buffers
     const uint32_t pfull_r = ptx::mapa(bar_addr<KVF>(base, B_PFULL), peer);
     const uint32_t sw = (uint32_t)(h & 7);
-    uint32_t g = 0, k = 0;  // pages, ring items
+    uint32_t g = 0, k = 0, segn = 0;  // pages, ring items, segments
+    uint32_t qbits = 0;               // parity of the next phase of each stage's query barrier
     bool ok = true;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
@@ -451,7 +507,8 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
         // 2c + h/64, i.e. 32 columns of bf16 pairs
         for (int qi = 0; qi < Q_ITEMS && ok; ++qi, ++k) {
             const uint32_t stage = k % STAGES;
-            if (!warp_wait(bar_addr<KVF>(base, B_FULL + stage), (k / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_FULL + stage), (qbits >> stage) & 1u, wc, false, lane)) { ok = false; break; }
+            qbits ^= 1u << stage;
 #pragma unroll 1
             for (int j = 0; j < 9; ++j) {
                 const int b = 9 * qi + j;
@@ -472,6 +529,10 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
         if (!ok) break;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
+        // both issuers saw the previous query's barrier phase, so none of them can find this
+        // one two phases ahead
+        if (segn > 0 && !warp_wait(bar_addr<KVF>(base, B_QSEEN), (segn - 1) & 1u, wc, false, lane)) { ok = false; break; }
+        ++segn;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_QREADY));
         float m_run = -INFINITY, l = 0.f;
@@ -521,8 +582,8 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             }
             l += sum;
             // P row h -> value CTA, 128-byte swizzled (16-byte chunk k at k ^ (h & 7))
-            const uint32_t pb = g & 1u;
-            if (!warp_wait(bar_addr<KVF>(base, B_PEMPTY + pb), (use & 1u) ^ 1u, wc, true, lane)) { ok = false; break; }
+            const uint32_t pb = g % NPBUF;
+            if (!warp_wait(bar_addr<KVF>(base, B_PEMPTY + pb), ((g / NPBUF) & 1u) ^ 1u, wc, true, lane)) { ok = false; break; }
             const uint32_t row = pbuf_r + pb * PBUF_BYTES + (uint32_t)h * 128u;
             const uint32_t fb = pfull_r + 8u * pb;
 #pragma unroll
@@ -540,19 +601,20 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
 // ----------------------------------------------------------------------------- value CTA
 template <int KVF>
 __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
-                                          const WaitCtl& wc) {
-    constexpr int STAGES = Lay<KVF>::STAGES;
+                                          const WaitCtl& wc, int lane) {
+    constexpr int STAGES = Lay<KVF>::VSTAGES;
     constexpr int OFF_R = Lay<KVF>::OFF_R;
+    constexpr uint32_t NPBUF = Lay<KVF>::NPBUF;
     uint32_t g = 0, segn = 0;
     bool ok = true;
     Segment sg;
     while (ok && c.next(a.qs, &sg)) {
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const bool first = pg == sg.page_begin;
-            const uint32_t stage = g % STAGES, pb = g & 1u;
-            if (!wait_bar(bar_addr<KVF>(base, B_FULL + stage), (g / STAGES) & 1u, wc)) { ok = false; break; }
-            if (!wait_bar(bar_addr<KVF>(base, B_PREADY + pb), (g >> 1) & 1u, wc)) { ok = false; break; }
-            if (first && segn > 0 && !wait_bar(bar_addr<KVF>(base, B_OFREE), (segn - 1) & 1u, wc)) { ok = false; break; }
+            const uint32_t stage = g % STAGES, pb = g % NPBUF;
+            if (!warp_wait(bar_addr<KVF>(base, B_FULL + stage), (g / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_PREADY + pb), (g / NPBUF) & 1u, wc, false, lane)) { ok = false; break; }
+            if (first && segn > 0 && !warp_wait(bar_addr<KVF>(base, B_OFREE), (segn - 1) & 1u, wc, false, lane)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint64_t da = ptx::desc_sw128(base + OFF_R + pb * PBUF_BYTES, 16, 1024);
             const uint64_t db = ptx::desc_sw128(base + stage * V_STAGE_BYTES, CHUNK, 1024);
@@ -560,28 +622,30 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // 16 tokens per MMA; V is MN-major: chunks 8 KB apart
-                    ptx::mma_ss(tmem + TM_O + hf * 256, da + (uint64_t)((kk * 32) >> 4),
+                    ptx::mma_ss_elect(tmem + TM_O + hf * 256, da + (uint64_t)((kk * 32) >> 4),
                                 db + (uint64_t)((hf * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV,
                                 (first && kk == 0) ? 0u : 1u);
             }
-            ptx::tc_commit(bar_addr<KVF>(base, B_PVDONE + pb));
-            ptx::tc_commit(bar_addr<KVF>(base, B_EMPTY + stage));
+            ptx::tc_commit_elect(bar_addr<KVF>(base, B_PVDONE + pb));
+            ptx::tc_commit_elect(bar_addr<KVF>(base, B_EMPTY + stage));
         }
         ++segn;
     }
     // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
     // whatever the configured limit (which may be microseconds when a caller tests timeouts)
-    ptx::tc_commit(bar_addr<KVF>(base, B_DONE));
+    __syncwarp();
+    ptx::tc_commit_elect(bar_addr<KVF>(base, B_DONE));
     WaitCtl w2 = wc;
     w2.ignore_abort = true;
     w2.limit_ns = 20000000ull;
-    wait_bar(bar_addr<KVF>(base, B_DONE), 0, w2);
+    warp_wait(bar_addr<KVF>(base, B_DONE), 0, w2, false, lane);
 }
 
 template <int KVF>
 __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem, int warp,
                                             int lane, const WaitCtl& wc) {
     constexpr int OFF_R = Lay<KVF>::OFF_R;
+    constexpr uint32_t NPBUF = Lay<KVF>::NPBUF;
     const int qd = warp & 3;
     const int h = qd * 32 + lane;
     const uint32_t tO = tmem + ((uint32_t)(qd * 32) << 16) + TM_O;
@@ -592,7 +656,7 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         float l_last = 0.f;
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
             const bool first = pg == sg.page_begin;
-            const uint32_t pb = g & 1u, use = g >> 1;
+            const uint32_t pb = g % NPBUF, use = g / NPBUF;
             if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(bar_addr<KVF>(base, B_PFULL + pb), PBUF_BYTES);
             if (!warp_wait(bar_addr<KVF>(base, B_PFULL + pb), use & 1u, wc, true, lane)) { ok = false; break; }
             const float2 meta = ptx::ld_shared_v2(base + OFF_R + pb * PBUF_BYTES + P_BYTES + (uint32_t)h * 8u);
@@ -600,9 +664,10 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
             const bool resc = !first && meta.x != 1.f;
             if (__any_sync(0xffffffffu, resc)) {
                 // O must be stable: the previous page's PV has completed.  pvdone is kept per P
-                // buffer so that no parity wait here is ever two phases away from its target.
+                // buffer so that no parity wait here is ever two phases away from its target
+                // (P of this page was sent after the PV of page g - NPBUF completed).
                 const uint32_t gp = g - 1;
-                if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + (gp & 1u)), (gp >> 1) & 1u, wc, false, lane)) {
+                if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + gp % NPBUF), (gp / NPBUF) & 1u, wc, false, lane)) {
                     ok = false;
                     break;
                 }
@@ -634,7 +699,7 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
         // drain O / l once the segment's last PV has completed
         {
             const uint32_t gl = g - 1;
-            if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + (gl & 1u)), (gl >> 1) & 1u, wc, false, lane)) { ok = false; break; }
+            if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + gl % NPBUF), (gl / NPBUF) & 1u, wc, false, lane)) { ok = false; break; }
         }
         ptx::tc_fence_after();
         const float inv_l = l_last > 0.f ? 1.f / l_last : 0.f;
@@ -690,13 +755,14 @@ __device__ __forceinline__ void value_warps(const AttnArgs& a, UnitCursor c, uin
 template <int KVF>
 __device__ __forceinline__ void value_release(const AttnArgs& a, UnitCursor c, uint32_t base, int lane,
                                               const WaitCtl& wc) {
+    constexpr uint32_t NPBUF = Lay<KVF>::NPBUF;
     const uint32_t pempty_r = ptx::mapa(bar_addr<KVF>(base, B_PEMPTY), 0);  // the score CTA's barriers
     uint32_t g = 0;
     Segment sg;
     while (c.next(a.qs, &sg)) {
         for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
-            if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + (g & 1u)), (g >> 1) & 1u, wc, false, lane)) return;
-            if (lane == 0) ptx::mbar_arrive_remote(pempty_r + 8u * (g & 1u));
+            if (!warp_wait(bar_addr<KVF>(base, B_PVDONE + g % NPBUF), (g / NPBUF) & 1u, wc, false, lane)) return;
+            if (lane == 0) ptx::mbar_arrive_remote(pempty_r + 8u * (g % NPBUF));
         }
     }
 }
@@ -726,10 +792,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < L::STAGES; ++s) {
+        for (int s = 0; s < (L::STAGES > L::VSTAGES ? L::STAGES : L::VSTAGES); ++s) {
             // MX caches: the four converter warps complete every stage (a query stage also
             // waits for the TMA's bytes)
             ptx::mbar_init(bar_addr<KVF>(base, B_FULL + s), KVF == KV_PLAIN ? 1 : 4);
+            ptx::mbar_init(bar_addr<KVF>(base, B_FULLP + 2 * s), KVF == KV_PLAIN ? 1 : 4);
+            ptx::mbar_init(bar_addr<KVF>(base, B_FULLP + 2 * s + 1), KVF == KV_PLAIN ? 1 : 4);
             ptx::mbar_init(bar_addr<KVF>(base, B_EMPTY + s), 1);
         }
         for (int s = 0; s < L::RAW_STAGES; ++s) {
@@ -739,14 +807,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr<KVF>(base, B_SFULL + b), 1);
             ptx::mbar_init(bar_addr<KVF>(base, B_SFREE + b), 4);
+        }
+        for (int b = 0; b < L::NPBUF; ++b) {
             ptx::mbar_init(bar_addr<KVF>(base, B_PFULL + b), 1);
             ptx::mbar_init(bar_addr<KVF>(base, B_PEMPTY + b), 1);
             ptx::mbar_init(bar_addr<KVF>(base, B_PREADY + b), 4);
             ptx::mbar_init(bar_addr<KVF>(base, B_PVDONE + b), 1);
         }
         ptx::mbar_init(bar_addr<KVF>(base, B_OFREE), 4);
-        ptx::mbar_init(bar_addr<KVF>(base, B_DONE), 1);
+        ptx::mbar_init(bar_addr<KVF>(base, B_DONE), rank == 0 ? 2 : 1);  // score CTA: two issuers
         ptx::mbar_init(bar_addr<KVF>(base, B_QREADY), 4);
+        ptx::mbar_init(bar_addr<KVF>(base, B_QSEEN), 2);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -774,14 +845,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 
     const WaitCtl wc{args.wait_ns, abort_flag, false};
 
     if (warp == 0) {
-        if (lane == 0) producer<KVF>(a, &tmap, &tmq, cur, base, rank, wc);
-    } else if (warp == 1) {
         if (lane == 0) {
-            if (rank == 0) score_mma<KVF>(a, cur, base, tmem, wc);
-            else value_mma<KVF>(a, cur, base, tmem, wc);
+            if (rank == 0) producer<KVF, L::STAGES>(a, &tmap, &tmq, cur, base, rank, wc);
+            else producer<KVF, L::VSTAGES>(a, &tmap, &tmq, cur, base, rank, wc);
         }
+    } else if (warp == 1) {
+        if (rank == 0) score_mma<KVF, 0>(a, cur, base, tmem, wc, lane);
+        else value_mma<KVF>(a, cur, base, tmem, wc, lane);
     } else if (warp == 6) {
         if (rank == 1) value_release<KVF>(a, cur, base, lane, wc);
+        else score_mma<KVF, 1>(a, cur, base, tmem, wc, lane);
     } else if (warp >= 7) {
         if (KVF != KV_PLAIN) converter<KVF>(a, &tmq, cur, base, rank, warp - 7, lane, wc);
     } else if (rank == 0) {

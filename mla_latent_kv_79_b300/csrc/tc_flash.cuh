@@ -226,13 +226,16 @@ __device__ __forceinline__ void f_producer(const FlashArgs& a, const CUtensorMap
 }
 
 // ----------------------------------------------------------------------------- warp 1: MMA
-__device__ __forceinline__ void f_mma(uint32_t base, uint32_t tmem, int n_t, const FWait& wc) {
-    bool ok = fwait(fbar(base, F_QFULL), 0, wc);
+// Run by the whole warp: every lane computes the descriptors, one elected lane issues (issuing
+// from a single active lane costs issue slots that the softmax warps on the same
+// sub-partitions need).
+__device__ __forceinline__ void f_mma(uint32_t base, uint32_t tmem, int n_t, const FWait& wc, int lane) {
+    bool ok = fwait_warp(fbar(base, F_QFULL), 0, wc, lane);
     const uint64_t qd = ptx::desc_sw128(base, 16, 1024);
     auto qk = [&](int j) -> bool {
         const int st = j & 1;
-        if (!fwait(fbar(base, F_KVFULL + st), (j >> 1) & 1, wc)) return false;
-        if (j >= 2 && !fwait(fbar(base, F_SFREE + st), ((j >> 1) & 1) ^ 1, wc)) return false;
+        if (!fwait_warp(fbar(base, F_KVFULL + st), (j >> 1) & 1, wc, lane)) return false;
+        if (j >= 2 && !fwait_warp(fbar(base, F_SFREE + st), ((j >> 1) & 1) ^ 1, wc, lane)) return false;
         ptx::tc_fence_after();
         const uint64_t kd = ptx::desc_sw128(base + OFF_KV + st * KV_STAGE, 16, 1024);
         const uint32_t d = tmem + TM_S + st * 128;
@@ -241,23 +244,23 @@ __device__ __forceinline__ void f_mma(uint32_t base, uint32_t tmem, int n_t, con
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t off = (uint64_t)((cc * BQ * 128 + kk * 32) >> 4);
-                ptx::mma_ss(d, qd + off, kd + off, IDESC_S, (cc | kk) ? 1u : 0u);
+                ptx::mma_ss_elect(d, qd + off, kd + off, IDESC_S, (cc | kk) ? 1u : 0u);
             }
-        ptx::tc_commit(fbar(base, F_SFULL + st));
+        ptx::tc_commit_elect(fbar(base, F_SFULL + st));
         return true;
     };
     auto pv = [&](int i) -> bool {
         const int st = i & 1;
-        if (!fwait(fbar(base, F_PFULL + st), (i >> 1) & 1, wc)) return false;
+        if (!fwait_warp(fbar(base, F_PFULL + st), (i >> 1) & 1, wc, lane)) return false;
         ptx::tc_fence_after();
         // V is the MN-major B operand: 64-column chunks 16 KB apart, 16 keys = 2 KB per MMA
         const uint64_t vd = ptx::desc_sw128(base + OFF_KV + st * KV_STAGE + K_BYTES, BKEY * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < BKEY / 16; ++kk)
-            ptx::mma_ts(tmem + TM_O, tmem + TM_P + st * 64 + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_O,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-        ptx::tc_commit(fbar(base, F_PVDONE + st));
-        ptx::tc_commit(fbar(base, F_KVEMPTY + st));
+            ptx::mma_ts_elect(tmem + TM_O, tmem + TM_P + st * 64 + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), IDESC_O,
+                              (i > 0 || kk > 0) ? 1u : 0u);
+        ptx::tc_commit_elect(fbar(base, F_PVDONE + st));
+        ptx::tc_commit_elect(fbar(base, F_KVEMPTY + st));
         return true;
     };
     for (int j = 0; ok && j < n_t; ++j) {
@@ -266,11 +269,12 @@ __device__ __forceinline__ void f_mma(uint32_t base, uint32_t tmem, int n_t, con
     }
     if (ok) pv(n_t - 1);
     // every MMA issued completes before TMEM is freed (a fixed 20 ms bound)
-    ptx::tc_commit(fbar(base, F_DONE));
+    __syncwarp();
+    ptx::tc_commit_elect(fbar(base, F_DONE));
     FWait w2 = wc;
     w2.ignore_abort = true;
     w2.limit_ns = 20000000ull;
-    fwait(fbar(base, F_DONE), 0, w2);
+    fwait_warp(fbar(base, F_DONE), 0, w2, lane);
 }
 
 // ----------------------------------------------------------------------------- warps 2-5
@@ -456,7 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (warp == 0) {
             if (lane == 0) f_producer(a, &tmq, &tmk, &tmr, &tmv, base, h, q0, n_t, wc);
         } else if (warp == 1) {
-            if (lane == 0) f_mma(base, tmem, n_t, wc);
+            f_mma(base, tmem, n_t, wc, lane);
         } else {
             f_softmax(a, base, tmem, h, q0, n_t, warp, lane, wc);
         }
