@@ -557,15 +557,20 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_SFREE + sb));
 
-            // scaled scores in log2 units; tokens past the sequence end are masked
+            // raw scores; tokens past the sequence end are masked (only the last page of a
+            // sequence has any, and the branch is warp-uniform).  The scale (log2 units) is
+            // positive, so it scales the maximum and folds into the exponent's FFMA.
             const int valid = sg.len - pg * PAGE;
-            float mx = -INFINITY;
+            if (valid < PAGE) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float x = j < valid ? s[j] * args.scale_log2 : -INFINITY;
-                s[j] = x;
-                mx = fmaxf(mx, x);
+                for (int j = 0; j < 64; ++j)
+                    if (j >= valid) s[j] = -INFINITY;
             }
+            float mr = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) mr = fmaxf(mr, s[j]);
+            const float c2 = args.scale_log2;
+            const float mx = mr * c2;
             float alpha = 1.f;
             if (mx > m_run + TAU) {
                 alpha = ptx::ex2(m_run - mx);
@@ -576,7 +581,7 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = ptx::ex2(s[2 * j] - m_run), p1 = ptx::ex2(s[2 * j + 1] - m_run);
+                const float p0 = ptx::ex2(fmaf(s[2 * j], c2, -m_run)), p1 = ptx::ex2(fmaf(s[2 * j + 1], c2, -m_run));
                 sum += p0 + p1;
                 pk[j] = ptx::pack_bf16(p0, p1);
             }
@@ -791,7 +796,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 
     const int unit = blockIdx.x >> 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
+    // Set-up runs side by side: warp 2 initialises the barriers, warp 1 allocates TMEM, and
+    // warp 0 computes the split schedule (its loads of the sequence lengths are the long pole).
+    if (threadIdx.x == 64) {
         for (int s = 0; s < (L::STAGES > L::VSTAGES ? L::STAGES : L::VSTAGES); ++s) {
             // MX caches: the four converter warps complete every stage (a query stage also
             // waits for the TMA's bytes)
@@ -829,19 +836,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 
         ptx::tmem_alloc(base + L::OFF_MISC, 512);
         ptx::tmem_relinquish();
     }
+    // Launched as a programmatic dependent, this kernel may start while the kernels before it
+    // (the absorption GEMM, and before that possibly a cache append) finish.  Lengths and page
+    // table come from earlier work and are read at once; both producers wait for the preceding
+    // grid (griddepcontrol.wait) before loading queries or cache rows.
+    UnitCursor cur;
+    long long per;
+    cur.init(a.qs, unit, a.n_units, red, &per);  // ends with a block barrier
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
-    // Launched as a programmatic dependent, this kernel may start while the kernels before it
-    // (the absorption GEMM, and before that possibly a cache append) finish.  Lengths and page
-    // table come from earlier work and are read at once; both producers wait for the preceding
-    // grid (griddepcontrol.wait) before loading queries or cache rows.
-
-    UnitCursor cur;
-    long long per;
-    cur.init(a.qs, unit, a.n_units, red, &per);
     const WaitCtl wc{args.wait_ns, abort_flag, false};
 
     if (warp == 0) {
