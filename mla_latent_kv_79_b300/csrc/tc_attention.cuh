@@ -86,7 +86,9 @@ enum {
     B_REMPTY = B_RFULL + MAX_RAW,    // MX caches: [RAW_STAGES] the 4 converter warps read it
     B_FULLP = B_REMPTY + MAX_RAW,    // score CTA: [STAGES][2] page of issuer i landed in a stage
     B_QSEEN = B_FULLP + 2 * MAX_STAGES,  // score CTA: both issuers saw the segment's query
-    NBARS = B_QSEEN + 1
+    B_DRYW = B_QSEEN + 1,            // never arrived on: a parity-1 wait passes (the dry pass)
+    B_DRYC = B_DRYW + 1,             // arrivals of the dry pass, never waited on
+    NBARS = B_DRYC + 1
 };
 static_assert(NBARS <= 64, "the producer tracks full barriers in 64-bit masks");
 
@@ -430,47 +432,72 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
                                           const WaitCtl& wc, int lane) {
     constexpr int STAGES = Lay<KVF>::STAGES;
     constexpr uint32_t sb = ISSUER;
+    const uint32_t dry_w = bar_addr<KVF>(base, B_DRYW), dry_c = bar_addr<KVF>(base, B_DRYC);
     uint32_t g = 0, k = 0, segn = 0;  // pages, ring items, segments
     uint32_t pbits = 0;               // parity of the next phase of this issuer's page barrier, per stage
     uint32_t uses = 0;                // pages issued into this issuer's score buffer
+    int pg = 0, pend = 0;             // the open segment's pages
     bool ok = true;
+    // The first pass is dry: the page body runs once at entry, on whatever the score buffer,
+    // the query columns and stage 0 hold, against barriers that pass at once or that nobody
+    // waits on.  Its code is then in the instruction caches when the first page lands (after
+    // an L2 flush that first pass costs several microseconds); the first real MMA of the
+    // buffer overwrites what it wrote, and the drain commit below covers its MMAs.
+    bool dry = true;
     Segment sg;
-    while (ok && c.next(a.qs, &sg)) {
-        // the softmax warps put the segment's query into TMEM columns [TM_Q, TM_Q + 288) (they
-        // do so only after reading the previous segment's last scores, i.e. after its QKs);
-        // then the stages that carried it are free
-        if (!warp_wait(bar_addr<KVF>(base, B_QREADY), segn & 1u, wc, false, lane)) break;
-        ptx::tc_fence_after();
-        if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_QSEEN));
-        if (ISSUER == 0)
-            for (int qi = 0; qi < Q_ITEMS; ++qi)
-                if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_EMPTY + (k + qi) % STAGES));
-        k += Q_ITEMS;
-        ++segn;
-        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g, ++k) {
-            if ((g & 1u) != sb) continue;  // the other issuer's page
-            const uint32_t stage = k % STAGES;
-            if (!warp_wait(bar_addr<KVF>(base, B_FULLP + 2 * stage + sb), (pbits >> stage) & 1u, wc, false, lane)) { ok = false; break; }
-            pbits ^= 1u << stage;
-            if (!warp_wait(bar_addr<KVF>(base, B_SFREE + sb), (uses & 1u) ^ 1u, wc, false, lane)) { ok = false; break; }
-            ++uses;
-            ptx::tc_fence_after();
-            // descriptors are the stage's base descriptor plus compile-time offsets (the 14-bit
-            // address field cannot carry: shared addresses are < 256 KB).  The 36 MMAs are fully
-            // unrolled: with a loop around them the issuing thread, not the tensor core, set the
-            // pace (measured on B300: about 85 cycles per N=64 MMA against 48 unrolled).
-            const uint64_t d_pg = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
-            const uint32_t d = tmem + TM_S + sb * 64;
-#pragma unroll
-            for (int cc = 0; cc < 9; ++cc) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA, 4 per 64-column chunk
-                    ptx::mma_ts_elect(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
-                                IDESC_QK, (cc | kk) ? 1u : 0u);
+    for (;;) {
+        uint32_t stage = 0;
+        if (!dry) {
+            // this issuer's next page, opening segments as the cursor yields them
+            bool found = false;
+            while (!found) {
+                if (pg >= pend) {
+                    if (!c.next(a.qs, &sg)) break;
+                    // the softmax warps put the segment's query into TMEM columns [TM_Q,
+                    // TM_Q + 288) (they do so only after reading the previous segment's last
+                    // scores, i.e. after its QKs); then the stages that carried it are free
+                    if (!warp_wait(bar_addr<KVF>(base, B_QREADY), segn & 1u, wc, false, lane)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_QSEEN));
+                    if (ISSUER == 0)
+                        for (int qi = 0; qi < Q_ITEMS; ++qi)
+                            if (lane == 0) ptx::mbar_arrive(bar_addr<KVF>(base, B_EMPTY + (k + qi) % STAGES));
+                    k += Q_ITEMS;
+                    ++segn;
+                    pg = sg.page_begin;
+                    pend = sg.page_end;
+                    continue;
+                }
+                if ((g & 1u) == sb) found = true;
+                else ++pg, ++g, ++k;  // the other issuer's page
             }
-            ptx::tc_commit_elect(bar_addr<KVF>(base, B_SFULL + sb));
-            ptx::tc_commit_elect(bar_addr<KVF>(base, B_EMPTY + stage));
+            if (!ok || !found) break;
+            stage = k % STAGES;
         }
+        const uint32_t bfull = dry ? dry_w : bar_addr<KVF>(base, B_FULLP + 2 * stage + sb);
+        if (!warp_wait(bfull, dry ? 1u : (pbits >> stage) & 1u, wc, false, lane)) break;
+        const uint32_t bsfree = dry ? dry_w : bar_addr<KVF>(base, B_SFREE + sb);
+        if (!warp_wait(bsfree, dry ? 1u : (uses & 1u) ^ 1u, wc, false, lane)) break;
+        pbits ^= dry ? 0u : 1u << stage;
+        uses += dry ? 0u : 1u;
+        ptx::tc_fence_after();
+        // descriptors are the stage's base descriptor plus compile-time offsets (the 14-bit
+        // address field cannot carry: shared addresses are < 256 KB).  The 36 MMAs are fully
+        // unrolled: with a loop around them the issuing thread, not the tensor core, set the
+        // pace (measured on B300: about 85 cycles per N=64 MMA against 48 unrolled).
+        const uint64_t d_pg = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
+        const uint32_t d = tmem + TM_S + sb * 64;
+#pragma unroll
+        for (int cc = 0; cc < 9; ++cc) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA, 4 per 64-column chunk
+                ptx::mma_ts_elect(d, tmem + TM_Q + cc * 32 + kk * 8, d_pg + (uint64_t)((cc * CHUNK + kk * 32) >> 4),
+                                  IDESC_QK, (cc | kk) ? 1u : 0u);
+        }
+        ptx::tc_commit_elect(dry ? dry_c : bar_addr<KVF>(base, B_SFULL + sb));
+        ptx::tc_commit_elect(dry ? dry_c : bar_addr<KVF>(base, B_EMPTY + stage));
+        if (!dry) ++pg, ++g, ++k;
+        dry = false;
     }
     // every MMA this thread issued completes before the CTA frees its TMEM (the drain barrier
     // counts both issuers): a fixed 20 ms bound, whatever the configured limit (which may be
@@ -610,31 +637,46 @@ __device__ __forceinline__ void value_mma(const AttnArgs& a, UnitCursor c, uint3
     constexpr int STAGES = Lay<KVF>::VSTAGES;
     constexpr int OFF_R = Lay<KVF>::OFF_R;
     constexpr uint32_t NPBUF = Lay<KVF>::NPBUF;
-    uint32_t g = 0, segn = 0;
-    bool ok = true;
+    const uint32_t dry_w = bar_addr<KVF>(base, B_DRYW), dry_c = bar_addr<KVF>(base, B_DRYC);
+    uint32_t g = 0, segn = 0;  // pages, segments opened
+    int pg = 0, pbeg = 0, pend = 0;
+    // The first pass is dry (as in the score issuers): one page's PV on whatever P buffer 0 and
+    // stage 0 hold, into O, which the first real page overwrites (its first MMA does not
+    // accumulate); the drain commit below covers it.
+    bool dry = true;
     Segment sg;
-    while (ok && c.next(a.qs, &sg)) {
-        for (int pg = sg.page_begin; pg < sg.page_end; ++pg, ++g) {
-            const bool first = pg == sg.page_begin;
-            const uint32_t stage = g % STAGES, pb = g % NPBUF;
-            if (!warp_wait(bar_addr<KVF>(base, B_FULL + stage), (g / STAGES) & 1u, wc, false, lane)) { ok = false; break; }
-            if (!warp_wait(bar_addr<KVF>(base, B_PREADY + pb), (g / NPBUF) & 1u, wc, false, lane)) { ok = false; break; }
-            if (first && segn > 0 && !warp_wait(bar_addr<KVF>(base, B_OFREE), (segn - 1) & 1u, wc, false, lane)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint64_t da = ptx::desc_sw128(base + OFF_R + pb * PBUF_BYTES, 16, 1024);
-            const uint64_t db = ptx::desc_sw128(base + stage * V_STAGE_BYTES, CHUNK, 1024);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // 16 tokens per MMA; V is MN-major: chunks 8 KB apart
-                    ptx::mma_ss_elect(tmem + TM_O + hf * 256, da + (uint64_t)((kk * 32) >> 4),
-                                db + (uint64_t)((hf * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV,
-                                (first && kk == 0) ? 0u : 1u);
+    for (;;) {
+        if (!dry) {
+            bool more = true;
+            while (pg >= pend) {
+                if (!c.next(a.qs, &sg)) { more = false; break; }
+                pg = pbeg = sg.page_begin;
+                pend = sg.page_end;
+                ++segn;
             }
-            ptx::tc_commit_elect(bar_addr<KVF>(base, B_PVDONE + pb));
-            ptx::tc_commit_elect(bar_addr<KVF>(base, B_EMPTY + stage));
+            if (!more) break;
         }
-        ++segn;
+        const bool first = dry || pg == pbeg;
+        const uint32_t stage = g % STAGES, pb = g % NPBUF;
+        if (!warp_wait(dry ? dry_w : bar_addr<KVF>(base, B_FULL + stage), dry ? 1u : (g / STAGES) & 1u, wc, false, lane)) break;
+        if (!warp_wait(dry ? dry_w : bar_addr<KVF>(base, B_PREADY + pb), dry ? 1u : (g / NPBUF) & 1u, wc, false, lane)) break;
+        // O of the previous segment is drained before this segment's first PV overwrites it
+        if (!dry && first && segn > 1 && !warp_wait(bar_addr<KVF>(base, B_OFREE), (segn - 2) & 1u, wc, false, lane)) break;
+        ptx::tc_fence_after();
+        const uint64_t da = ptx::desc_sw128(base + OFF_R + pb * PBUF_BYTES, 16, 1024);
+        const uint64_t db = ptx::desc_sw128(base + stage * V_STAGE_BYTES, CHUNK, 1024);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // 16 tokens per MMA; V is MN-major: chunks 8 KB apart
+                ptx::mma_ss_elect(tmem + TM_O + hf * 256, da + (uint64_t)((kk * 32) >> 4),
+                                  db + (uint64_t)((hf * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV,
+                                  (first && kk == 0) ? 0u : 1u);
+        }
+        ptx::tc_commit_elect(dry ? dry_c : bar_addr<KVF>(base, B_PVDONE + pb));
+        ptx::tc_commit_elect(dry ? dry_c : bar_addr<KVF>(base, B_EMPTY + stage));
+        if (!dry) ++pg, ++g;
+        dry = false;
     }
     // every MMA this thread issued completes before the CTA frees its TMEM: a fixed 20 ms bound,
     // whatever the configured limit (which may be microseconds when a caller tests timeouts)
@@ -825,6 +867,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<KVF>::NTHREADS, 
         ptx::mbar_init(bar_addr<KVF>(base, B_DONE), rank == 0 ? 2 : 1);  // score CTA: two issuers
         ptx::mbar_init(bar_addr<KVF>(base, B_QREADY), 4);
         ptx::mbar_init(bar_addr<KVF>(base, B_QSEEN), 2);
+        ptx::mbar_init(bar_addr<KVF>(base, B_DRYW), 1);
+        ptx::mbar_init(bar_addr<KVF>(base, B_DRYC), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
