@@ -93,10 +93,12 @@ enum {
 static_assert(NBARS <= 64, "the producer tracks full barriers in 64-bit masks");
 
 // Shared-memory layout per cache format (KVF: KV_PLAIN, KV_MXFP8, KV_MXFP4).  Both CTAs of a
-// pair use the same offsets.  The plain cache streams bf16 pages by TMA into a 3-stage ring.
-// An MX cache streams raw half pages (codes, then the 32 rows' scale bytes) by bulk copy into
-// a raw ring; four converter warps widen them into a 2-stage bf16 ring of the same layout as
-// the TMA writes, so the MMA and softmax code is shared.
+// pair use the same offsets.  The plain cache streams bf16 pages by TMA into a 3-stage ring in
+// the score CTA and a 2-stage one (the latent columns) in the value CTA, which keeps four P
+// buffers.  An MX cache streams raw half pages (codes, then the 32 rows' scale bytes) by bulk
+// copy into a raw ring; four converter warps widen them into a 2-stage bf16 ring of the same
+// layout as the TMA writes, so the MMA and softmax code is shared (two P buffers: the raw
+// ring takes the rest of shared memory).
 template <int KVF>
 struct Lay {
     static constexpr int STAGES = KVF == KV_PLAIN ? 3 : 2;         // score CTA ring
@@ -421,12 +423,12 @@ __device__ __forceinline__ void converter(const AttnArgs& a, const CUtensorMap* 
 }
 
 // ----------------------------------------------------------------------------- score CTA
-// Two issuing threads (warp 1 and warp 6, lane 0) split the pages: ISSUER takes the pages with
-// page index % 2 == ISSUER, always into score buffer ISSUER.  One thread issuing all 36 MMAs of
-// a page was the pace setter (about 88 cycles per N=64 MMA beside the softmax warps); two
-// threads keep the tensor pipe fed.  Each waits only on its own barriers: a page's full
-// barrier of (stage, issuer), its score buffer's free barrier, and the query barriers, which
-// both see every phase of (QSEEN keeps the next query out of TMEM until both saw this one).
+// Two issuing warps (warps 1 and 6, one elected lane issuing) split the pages: ISSUER takes the
+// pages with page index % 2 == ISSUER, always into score buffer ISSUER.  One thread issuing all
+// 36 MMAs of a page was the pace setter (about 88 cycles per N=64 MMA beside the softmax
+// warps).  Each waits only on its own barriers: a page's full barrier of (stage, issuer), its
+// score buffer's free barrier, and the query barriers, which both see every phase of (QSEEN
+// keeps the next query out of TMEM until both saw this one).
 template <int KVF, int ISSUER>
 __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint32_t base, uint32_t tmem,
                                           const WaitCtl& wc, int lane) {
@@ -484,7 +486,8 @@ __device__ __forceinline__ void score_mma(const AttnArgs& a, UnitCursor c, uint3
         // descriptors are the stage's base descriptor plus compile-time offsets (the 14-bit
         // address field cannot carry: shared addresses are < 256 KB).  The 36 MMAs are fully
         // unrolled: with a loop around them the issuing thread, not the tensor core, set the
-        // pace (measured on B300: about 85 cycles per N=64 MMA against 48 unrolled).
+        // pace (measured on B300 with one issuing lane: about 85 cycles per N=64 MMA against
+        // 48 unrolled).
         const uint64_t d_pg = ptx::desc_sw128(base + stage * S_STAGE_BYTES, 16, 1024);
         const uint32_t d = tmem + TM_S + sb * 64;
 #pragma unroll
