@@ -93,12 +93,34 @@ KERNEL_SOURCES = {
 }
 
 
-def source_digest(kernel_key=None):
-    """Digest of a kernel's sources (all of csrc/ when kernel_key is None)."""
-    h = hashlib.sha256()
+def code_text(src: str) -> str:
+    """C++/CUDA source without its comments, trailing blanks and empty lines: what the
+    compiler sees, so that an edit of a comment keeps a kernel's digest.  (String literals
+    hold no comment markers in these sources; the inline PTX uses none.)"""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            j = min([k for k in (src.find("//", i), src.find("/*", i)) if k >= 0] or [n])
+            out.append(src[i:j])
+            i = j
+    lines = [l.rstrip() for l in "".join(out).split("\n")]
+    return "\n".join(l for l in lines if l)
+
+
+def source_digest(kernel_key=None, read=None):
+    """Digest of a kernel's sources (all of csrc/ when kernel_key is None), comments left out.
+    `read(name)` returns a file's text (default: the working tree's)."""
     csrc = os.path.join(ROOT, "mla_latent_kv_79_b300", "csrc")
+    read = read or (lambda f: open(os.path.join(csrc, f)).read())
+    h = hashlib.sha256()
     for f in KERNEL_SOURCES.get(kernel_key) or sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(code_text(read(f)).encode())
     return h.hexdigest()[:16]
 
 

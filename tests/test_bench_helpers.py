@@ -41,6 +41,18 @@ def test_source_digest_is_per_kernel():
             assert os.path.exists(os.path.join(ROOT, "mla_latent_kv_79_b300", "csrc", f)), f
 
 
+def test_code_text_drops_comments_only():
+    src = "int a; // one\n/* two\n three */ int b;  \n\n  // four\nint c = 1 / 2;\n"
+    assert bench.code_text(src) == "int a;\n int b;\nint c = 1 / 2;"
+    # a comment edit keeps the digest, a code edit does not
+    base = {f: "int x = 1; // note\n" for f in bench.KERNEL_SOURCES["tc_flash"]}
+    d0 = bench.source_digest("tc_flash", read=lambda f: base[f])
+    reworded = dict(base, **{"tc_flash.cuh": "int x = 1; // another note\n/* and more */\n"})
+    changed = dict(base, **{"tc_flash.cuh": "int x = 2; // note\n"})
+    assert bench.source_digest("tc_flash", read=lambda f: reworded[f]) == d0
+    assert bench.source_digest("tc_flash", read=lambda f: changed[f]) != d0
+
+
 def _write_profile(d, digest, nbytes=12345):
     p = d / "tc_attention_decode_b16_l4096.md"
     p.write_text(f"# capture\n\n- dram_bytes_per_launch: {nbytes}\n- source_digest: {digest} (of some files)\n")
