@@ -616,9 +616,19 @@ __device__ __forceinline__ void score_softmax(const TcArgs& args, UnitCursor c, 
                 pk[j] = ptx::pack_bf16(p0, p1);
             }
             l += sum;
-            // P row h -> value CTA, 128-byte swizzled (16-byte chunk k at k ^ (h & 7))
+            // P row h -> value CTA, 128-byte swizzled (16-byte chunk k at k ^ (h & 7)).  P
+            // buffers come back in page order (the PVs complete in order and one warp hands them
+            // back), so an even page waits for the next page's buffer, which covers its own, and
+            // an odd page waits for nothing: one wait per two pages, always on the odd buffers,
+            // each of which sees every phase.
             const uint32_t pb = g % NPBUF;
-            if (!warp_wait(bar_addr<KVF>(base, B_PEMPTY + pb), ((g / NPBUF) & 1u) ^ 1u, wc, true, lane)) { ok = false; break; }
+            if ((g & 1u) == 0) {
+                const uint32_t gn = g + 1;
+                if (!warp_wait(bar_addr<KVF>(base, B_PEMPTY + gn % NPBUF), ((gn / NPBUF) & 1u) ^ 1u, wc, true, lane)) {
+                    ok = false;
+                    break;
+                }
+            }
             const uint32_t row = pbuf_r + pb * PBUF_BYTES + (uint32_t)h * 128u;
             const uint32_t fb = pfull_r + 8u * pb;
 #pragma unroll
