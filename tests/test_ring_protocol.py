@@ -201,3 +201,92 @@ def test_simpler_protocols_fail(shared_full, qseen):
         except (Spurious, Deadlock):
             return
     pytest.fail("no schedule exposed the simpler protocol")
+
+
+def run_p_ring(n_pages, npbuf, rnd, rule):
+    """The value CTA's P buffers: the softmax writes page g's P into buffer g % npbuf; the PVs
+    complete in page order (one thread issues them and each commit covers all its earlier
+    MMAs); a release warp waits for each PV in order and then arrives on the buffer's empty
+    barrier (in the kernel a remote arrive with release semantics, waited on with a
+    cluster-scope acquire, so a later buffer's phase also shows the earlier arrivals).
+    rule "pairs" is the kernel's: an even page waits for the next page's buffer, which covers
+    its own, and an odd page waits for nothing; "every" waits for each page's own buffer;
+    "even_own" (wrong) waits only on even pages, for their own buffer.  Raises if a wait passes
+    early or P is written over a buffer whose PV is still pending."""
+    empty = [Bar(1) for _ in range(npbuf)]
+    full = [Bar(1) for _ in range(npbuf)]
+    pv_done = [False] * n_pages
+    events, now, last_pv = [], [0], [0]
+
+    def later(fn, at=None):
+        events.append((at if at is not None else now[0] + rnd.randint(1, 30), fn))
+
+    def wait(bar, phase):
+        while not bar.try_wait(phase):
+            yield
+
+    def softmax_warps():
+        for g in range(n_pages):
+            for _ in range(rnd.randint(0, 6)):
+                yield
+            gw = {"every": g, "pairs": g + 1 if g % 2 == 0 else None,
+                  "even_own": g if g % 2 == 0 else None}[rule]
+            if gw is not None and gw >= npbuf:
+                yield from wait(empty[gw % npbuf], gw // npbuf - 1)
+            if g >= npbuf and not pv_done[g - npbuf]:
+                raise Spurious(f"P of page {g} written while the PV of page {g - npbuf} is pending")
+            later(lambda b=g % npbuf: full[b].arrive())  # the st.async bytes land
+
+    def value_mma():
+        for g in range(n_pages):
+            yield from wait(full[g % npbuf], g // npbuf)
+            for _ in range(rnd.randint(0, 8)):
+                yield
+            last_pv[0] = max(now[0] + rnd.randint(1, 30), last_pv[0] + 1)  # in page order
+            later(lambda g=g: pv_done.__setitem__(g, True), at=last_pv[0])
+
+    def release_warp():
+        for g in range(n_pages):
+            while not pv_done[g]:
+                yield
+            for _ in range(rnd.randint(0, 4)):
+                yield
+            empty[g % npbuf].arrive()
+
+    parties = [softmax_warps(), value_mma(), release_warp()]
+    alive = list(parties)
+    steps = 0
+    while alive or events:
+        steps += 1
+        if steps > 200_000:
+            raise Deadlock(f"{n_pages} pages")
+        now[0] += 1
+        for e in [e for e in events if e[0] <= now[0]]:
+            events.remove(e)
+            e[1]()
+        rnd.shuffle(alive)
+        for p in (alive[: rnd.randint(1, len(alive))] if alive else []):
+            try:
+                next(p)
+            except StopIteration:
+                alive.remove(p)
+    assert all(pv_done)
+
+
+@pytest.mark.parametrize("npbuf", [2, 4])
+def test_p_buffer_waits_every_other_page(npbuf):
+    for seed in range(200):
+        rnd = random.Random(seed)
+        run_p_ring(rnd.randint(1, 40), npbuf, rnd, "pairs")
+        run_p_ring(rnd.randint(1, 40), npbuf, rnd, "every")
+
+
+def test_p_buffer_wrong_rule_fails():
+    """Waiting on even pages for their own buffer only leaves the odd pages unguarded."""
+    for seed in range(200):
+        rnd = random.Random(seed)
+        try:
+            run_p_ring(rnd.randint(8, 40), 4, rnd, "even_own")
+        except Spurious:
+            return
+    pytest.fail("no schedule exposed the wrong rule")
